@@ -1,0 +1,84 @@
+"""Seeded synthetic inputs for the EXL3 linear layer.
+
+This module only draws random numbers.  It holds none of the layer's
+arithmetic, so both the CUDA path's tests and the CPU oracle can consume
+the same inputs without sharing any of the method.
+
+Distributions follow the workloads quoted for the layer:
+
+* trellis words: uniform over all 2^16 int16 bit patterns, shape
+  ``[K/16, N/16, 16*bits]`` (cuda-exl3 README, "VRAM"; TensorFold PR,
+  "What it adds");
+* suh / svh: fp16 ``sign * U(0.8, 1.2)`` with a fair random sign;
+* activations x: bf16 draws of N(0, 1).
+
+Everything is generated on the CPU with ``torch.Generator`` so that a
+given seed yields the same bytes on every machine; callers move tensors
+to the device themselves.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import List, Sequence
+
+import torch
+
+
+@dataclass
+class Layer:
+    """Host copies of one (possibly fused) EXL3 linear layer."""
+
+    k: int
+    shard_cols: List[int]  # column offsets, len S+1, shard s owns [c_s, c_{s+1})
+    bits: int
+    codebook: int  # 0 = 3inst, 1 = mcg, 2 = mul1
+    trellis: torch.Tensor  # int16 [K/16, N/16, 16*bits]
+    suh: torch.Tensor  # fp16 [S, K]
+    svh: torch.Tensor  # fp16 [N]
+
+    @property
+    def n(self) -> int:
+        return self.shard_cols[-1]
+
+    @property
+    def num_shards(self) -> int:
+        return len(self.shard_cols) - 1
+
+
+def _signed_uniform(g: torch.Generator, shape: Sequence[int]) -> torch.Tensor:
+    mag = torch.rand(shape, generator=g, dtype=torch.float64) * 0.4 + 0.8
+    sign = torch.randint(0, 2, shape, generator=g, dtype=torch.int64) * 2 - 1
+    return (mag * sign).to(torch.float16)
+
+
+def random_trellis(k: int, n: int, bits: int, g: torch.Generator) -> torch.Tensor:
+    """Uniform random int16 words, every bit pattern equally likely."""
+    if k % 16 or n % 16:
+        raise ValueError("k and n must be multiples of 16")
+    words = torch.randint(0, 1 << 16, (k // 16, n // 16, 16 * bits), generator=g, dtype=torch.int64)
+    return (words - (1 << 16) * (words >= (1 << 15))).to(torch.int16)
+
+
+def make_layer(k: int, shard_widths: Sequence[int], bits: int, codebook: int, seed: int) -> Layer:
+    g = torch.Generator().manual_seed(seed)
+    cols = [0]
+    for w in shard_widths:
+        cols.append(cols[-1] + int(w))
+    n = cols[-1]
+    trellis = random_trellis(k, n, bits, g)
+    suh = _signed_uniform(g, (len(shard_widths), k))
+    svh = _signed_uniform(g, (n,))
+    return Layer(k=k, shard_cols=cols, bits=bits, codebook=codebook, trellis=trellis, suh=suh, svh=svh)
+
+
+def make_x(m: int, k: int, seed: int) -> torch.Tensor:
+    """bf16 activations drawn from N(0, 1); smaller batches take a prefix."""
+    g = torch.Generator().manual_seed(seed + 7919)
+    return torch.randn((m, k), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def random_words(count: int, seed: int) -> torch.Tensor:
+    """Uniform int16 words (used for tile-level unpack tests)."""
+    g = torch.Generator().manual_seed(seed)
+    w = torch.randint(0, 1 << 16, (count,), generator=g, dtype=torch.int64)
+    return (w - (1 << 16) * (w >= (1 << 15))).to(torch.int16)
