@@ -1,0 +1,188 @@
+"""ctypes binding of libexl3.so (argument marshalling only).
+
+Every function takes torch tensors that already live on the GPU, checks
+dtype/contiguity/device, and passes raw pointers, sizes and the current CUDA
+stream to the C ABI.  All arithmetic happens in the library's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libexl3.so")
+_lib: Optional[ctypes.CDLL] = None
+
+CODEBOOKS = {"3inst": 0, "mcg": 1, "mul1": 2}
+_F16, _BF16 = 0, 1
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "split-k workspace too small", 4: "CUDA error"}
+
+
+class Exl3Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = ": " + _lib.exl3_last_error().decode()
+        super().__init__(f"{what} failed: {_STATUS.get(status, status)}{detail}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libexl3.so (built in-tree by ``build_ext.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise ImportError(
+            f"{_LIB_PATH} is missing: build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` (nvcc, sm_103a)"
+        )
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    L.exl3_input_transform.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
+    L.exl3_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, ctypes.c_int, i64, vp]
+    L.exl3_gemm_splitk.argtypes = L.exl3_gemm.argtypes[:-1] + [vp, sz, vp]
+    L.exl3_splitk_parts.argtypes = [i64, i64]
+    L.exl3_splitk_parts.restype = i32
+    L.exl3_splitk_workspace_bytes.argtypes = [i64, i64, i64]
+    L.exl3_splitk_workspace_bytes.restype = sz
+    L.exl3_test_codebook.argtypes = [ctypes.c_int, vp, vp]
+    L.exl3_test_unpack.argtypes = [vp, i32, ctypes.c_int, i64, i64, vp, vp]
+    L.exl3_status_string.argtypes = [ctypes.c_int]
+    L.exl3_status_string.restype = ctypes.c_char_p
+    L.exl3_last_error.argtypes = []
+    L.exl3_last_error.restype = ctypes.c_char_p
+    for name in ("exl3_input_transform", "exl3_gemm", "exl3_gemm_splitk", "exl3_test_codebook", "exl3_test_unpack"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().exl3_status_string(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise Exl3Error(status, what)
+
+
+def _stream(t: torch.Tensor):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cols(shard_cols: Sequence[int]):
+    arr = (ctypes.c_int32 * len(shard_cols))(*[int(c) for c in shard_cols])
+    return arr, len(shard_cols) - 1
+
+
+def splitk_parts(k: int, n: int) -> int:
+    return int(lib().exl3_splitk_parts(k, n))
+
+
+def splitk_workspace_bytes(m: int, k: int, n: int) -> int:
+    return int(lib().exl3_splitk_workspace_bytes(m, k, n))
+
+
+def input_transform(x: torch.Tensor, suh: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """xh[s] = fp16(H(x * suh[s]) * 2^-4) for every shard; x bf16/fp16 [m, k], suh fp16 [S, k]."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be bf16 or fp16")
+    _need(x, x.dtype, "x")
+    _need(suh, torch.float16, "suh")
+    m, k = x.shape
+    s = suh.shape[0]
+    if out is None:
+        out = torch.empty((s, m, k), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, "out")
+    st = lib().exl3_input_transform(_ptr(x), _BF16 if x.dtype == torch.bfloat16 else _F16, m, k, _ptr(suh), s,
+                                    _ptr(out), _stream(x))
+    _check(st, "exl3_input_transform")
+    return out
+
+
+def _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out):
+    _need(xh, torch.float16, "xh")
+    _need(trellis, torch.int16, "trellis")
+    _need(svh, torch.float16, "svh")
+    s, m, k = xh.shape
+    n = int(shard_cols[-1])
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=xh.device)
+    if out.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("output must be bf16 or fp16")
+    _need(out, out.dtype, "out")
+    cols, ns = _cols(shard_cols)
+    if ns != s:
+        raise ValueError("xh holds one slice per shard")
+    cbid = CODEBOOKS[cb] if isinstance(cb, str) else int(cb)
+    return m, k, n, cols, ns, cbid, out
+
+
+def gemm(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor, shard_cols: Sequence[int],
+         out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    m, k, n, cols, ns, cbid, out = _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+    st = lib().exl3_gemm(_ptr(xh), m, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(out),
+                         _BF16 if out.dtype == torch.bfloat16 else _F16, n, _stream(xh))
+    _check(st, "exl3_gemm")
+    return out
+
+
+def gemm_splitk(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor,
+                shard_cols: Sequence[int], acc: torch.Tensor, out_dtype=torch.bfloat16,
+                out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Split-k variant; ``acc`` is a zeroed fp32 workspace of at least splitk_workspace_bytes."""
+    m, k, n, cols, ns, cbid, out = _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+    _need(acc, torch.float32, "acc")
+    st = lib().exl3_gemm_splitk(_ptr(xh), m, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(out),
+                                _BF16 if out.dtype == torch.bfloat16 else _F16, n, _ptr(acc),
+                                acc.numel() * 4, _stream(xh))
+    _check(st, "exl3_gemm_splitk")
+    return out
+
+
+def linear(x: torch.Tensor, trellis: torch.Tensor, bits: int, cb, suh: torch.Tensor, svh: torch.Tensor,
+           shard_cols: Sequence[int], out_dtype=torch.bfloat16, acc: Optional[torch.Tensor] = None,
+           xh: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Whole layer: input rotation, then the GEMM (split-k when ``acc`` is given)."""
+    xh = input_transform(x, suh, xh)
+    if acc is not None:
+        return gemm_splitk(xh, trellis, bits, cb, svh, shard_cols, acc, out_dtype, out)
+    return gemm(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+
+
+def test_codebook(cb, device="cuda") -> torch.Tensor:
+    """fp16 bit patterns (as int16) of the codebook at all 65,536 states."""
+    out = torch.empty(65536, dtype=torch.int16, device=device)
+    cbid = CODEBOOKS[cb] if isinstance(cb, str) else int(cb)
+    _check(lib().exl3_test_codebook(cbid, _ptr(out), _stream(out)), "exl3_test_codebook")
+    return out
+
+
+def test_unpack(trellis: torch.Tensor, bits: int, cb) -> torch.Tensor:
+    """Dense Wq [k, n] (fp16 bit patterns as int16) decoded by the library."""
+    _need(trellis, torch.int16, "trellis")
+    kt, nt, w = trellis.shape
+    if w != 16 * bits:
+        raise ValueError("trellis last axis must be 16*bits")
+    out = torch.empty((16 * kt, 16 * nt), dtype=torch.int16, device=trellis.device)
+    cbid = CODEBOOKS[cb] if isinstance(cb, str) else int(cb)
+    st = lib().exl3_test_unpack(_ptr(trellis), bits, cbid, 16 * kt, 16 * nt, _ptr(out), _stream(trellis))
+    _check(st, "exl3_test_unpack")
+    return out

@@ -1,0 +1,175 @@
+// exl3_api.cu -- the C ABI declared in include/exl3.h: host-side validation,
+// the shape-only split-k policy, and dispatch to the kernels.  Nothing here
+// allocates device memory or synchronises the host.
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/exl3.h"
+#include "exl3_launch.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+// Largest batch a call accepts (keeps every grid dimension within CUDA's limits).
+constexpr int64_t kMaxRows = int64_t(1) << 22;
+
+exl3_status_t cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return EXL3_OK;
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+  return EXL3_ECUDA;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_kn(int64_t v) { return v >= 128 && v % 128 == 0 && v <= (int64_t(1) << 31); }
+
+bool valid_cb(int cb) { return cb == EXL3_CB_3INST || cb == EXL3_CB_MCG || cb == EXL3_CB_MUL1; }
+
+bool valid_dtype(int d) { return d == EXL3_F16 || d == EXL3_BF16; }
+
+// Shard edges: 0 = c_0 < c_1 < ... < c_S = n, every edge a multiple of 128
+// (cuda-exl3 README, "Loading into a dim vLLM has padded": Hadamard blocks are
+// whole 128-column blocks; "Notes on the format": one suh row per shard).
+bool valid_shards(const int32_t* cols, int32_t s, int64_t n) {
+  if (cols == nullptr || s < 1 || s > EXL3_MAX_SHARDS) return false;
+  if (cols[0] != 0 || cols[s] != n) return false;
+  for (int i = 0; i < s; ++i) {
+    if (cols[i + 1] <= cols[i] || cols[i + 1] % 128 != 0) return false;
+  }
+  return true;
+}
+
+// Validates everything exl3_gemm and exl3_gemm_splitk share and fills `a`.
+exl3_status_t check_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
+                         exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
+                         void* y, exl3_dtype_t y_dtype, int64_t n, exl3::GemmArgs* a) {
+  if (m < 0 || m > kMaxRows) return EXL3_EINVAL;
+  if (!valid_kn(k) || !valid_kn(n)) return EXL3_EINVAL;
+  if (bits < 1 || bits > 8 || !valid_cb(cb) || !valid_dtype(y_dtype)) return EXL3_EINVAL;
+  if (!valid_shards(shard_cols, num_shards, n)) return EXL3_EINVAL;
+  if (!aligned16(trellis) || !aligned16(svh)) return EXL3_EINVAL;
+  // an empty batch dereferences no activation or output, which may then be NULL
+  if (m > 0 && (!aligned16(xh) || !aligned16(y))) return EXL3_EINVAL;
+  memset(a, 0, sizeof(*a));
+  a->xh = xh;
+  a->trellis = trellis;
+  a->svh = svh;
+  a->y = y;
+  a->m = m;
+  a->k = k;
+  a->n = n;
+  a->num_shards = num_shards;
+  for (int i = 0; i <= num_shards; ++i) a->shard_cols[i] = shard_cols[i];
+  a->parts = 1;
+  a->y_bf16 = (y_dtype == EXL3_BF16) ? 1 : 0;
+  return EXL3_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+exl3_status_t exl3_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t m, int64_t k, const uint16_t* suh,
+                                   int32_t num_shards, uint16_t* xh, void* stream) {
+  if (m < 0 || m > kMaxRows || !valid_kn(k) || !valid_dtype(x_dtype)) return EXL3_EINVAL;
+  if (num_shards < 1 || num_shards > EXL3_MAX_SHARDS) return EXL3_EINVAL;
+  if (!aligned16(suh)) return EXL3_EINVAL;
+  if (m == 0) return EXL3_OK;  // empty batch: x and xh may be NULL
+  if (!aligned16(x) || !aligned16(xh)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_input_transform(x, x_dtype == EXL3_BF16, m, k, suh, num_shards, xh,
+                                                  static_cast<cudaStream_t>(stream)),
+                     "exl3_input_transform");
+}
+
+exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
+                        exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
+                        void* y, exl3_dtype_t y_dtype, int64_t n, void* stream) {
+  exl3::GemmArgs a;
+  exl3_status_t st = check_gemm(xh, m, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
+  if (st != EXL3_OK) return st;
+  if (m == 0) return EXL3_OK;
+  return cuda_status(exl3::launch_gemm_mma(a, bits, cb, static_cast<cudaStream_t>(stream)), "exl3_gemm");
+}
+
+// Shape-only split policy: the number of parts P makes (n/128) * P work units
+// fill the 152 SMs of a GB300 in whole waves as evenly as possible.  It is the
+// smallest P whose wave efficiency units / (152 * ceil(units / 152)) reaches
+// 0.85, else the most efficient P; P <= k/128 (parts are whole 128-row blocks)
+// and P <= 16.  It never depends on m, so rows are byte-equal across batches.
+int32_t exl3_splitk_parts(int64_t k, int64_t n) {
+  if (!valid_kn(k) || !valid_kn(n)) return 0;
+  const int64_t nb = n / 128;
+  const int64_t kb = k / 128;
+  const int64_t sms = 152;
+  const int64_t pmax = kb < 16 ? kb : 16;
+  int64_t best = 1;
+  double best_eff = -1.0;
+  for (int64_t p = 1; p <= pmax; ++p) {
+    const int64_t units = nb * p;
+    const double eff = (double)units / (double)(sms * ((units + sms - 1) / sms));
+    if (eff >= 0.85) return (int32_t)p;
+    if (eff > best_eff + 1e-12) {
+      best_eff = eff;
+      best = p;
+    }
+  }
+  return (int32_t)best;
+}
+
+size_t exl3_splitk_workspace_bytes(int64_t m, int64_t k, int64_t n) {
+  const int32_t p = exl3_splitk_parts(k, n);
+  if (p <= 0 || m < 0) return 0;
+  return (size_t)p * (size_t)m * (size_t)n * sizeof(float);
+}
+
+exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
+                               exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols,
+                               int32_t num_shards, void* y, exl3_dtype_t y_dtype, int64_t n, float* acc,
+                               size_t acc_bytes, void* stream) {
+  exl3::GemmArgs a;
+  exl3_status_t st = check_gemm(xh, m, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
+  if (st != EXL3_OK) return st;
+  if (m == 0) return EXL3_OK;
+  if (!aligned16(acc)) return EXL3_EINVAL;
+  if (acc_bytes < exl3_splitk_workspace_bytes(m, k, n)) return EXL3_EWORKSPACE;
+  a.acc = acc;
+  a.parts = exl3_splitk_parts(k, n);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.parts == 1) {
+    // one part: the fused epilogue already does everything; acc stays zero
+    return cuda_status(exl3::launch_gemm_mma(a, bits, cb, s), "exl3_gemm_splitk");
+  }
+  st = cuda_status(exl3::launch_gemm_mma(a, bits, cb, s), "exl3_gemm_splitk parts");
+  if (st != EXL3_OK) return st;
+  return cuda_status(exl3::launch_splitk_epilogue(a, s), "exl3_gemm_splitk epilogue");
+}
+
+exl3_status_t exl3_test_codebook(exl3_codebook_t cb, uint16_t* out, void* stream) {
+  if (!valid_cb(cb) || !aligned16(out)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_test_codebook(cb, out, static_cast<cudaStream_t>(stream)), "exl3_test_codebook");
+}
+
+exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebook_t cb, int64_t k, int64_t n,
+                               uint16_t* wq, void* stream) {
+  if (bits < 1 || bits > 8 || !valid_cb(cb)) return EXL3_EINVAL;
+  if (k < 16 || n < 16 || k % 16 || n % 16 || k > (int64_t(1) << 31) || n > (int64_t(1) << 31)) return EXL3_EINVAL;
+  if (!aligned16(trellis) || !aligned16(wq)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_test_unpack(trellis, bits, cb, k, n, wq, static_cast<cudaStream_t>(stream)),
+                     "exl3_test_unpack");
+}
+
+const char* exl3_status_string(exl3_status_t status) {
+  switch (status) {
+    case EXL3_OK: return "ok";
+    case EXL3_EINVAL: return "invalid argument";
+    case EXL3_EUNSUPPORTED: return "unsupported";
+    case EXL3_EWORKSPACE: return "split-k workspace too small";
+    case EXL3_ECUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* exl3_last_error(void) { return g_last_error; }
+
+}  // extern "C"

@@ -1,0 +1,196 @@
+// exl3_device.cuh -- device-side building blocks shared by the EXL3 kernels:
+// trellis windows, the three procedural codebooks, packed half2 output in
+// mma.m16n8k16 B-fragment order, and the 128-point butterfly.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace exl3 {
+
+// ---------------------------------------------------------------------------
+// Codebook constants.
+// mcg multiplier: cuda-exl3 README, "GLM-5.3-Flash" (multiplier 0xCBAC1FED).
+// 3inst / mul1: the pages print no constants; this library reads 3inst as the
+// mcg multiply with an increment of 1 and mul1 as the same multiplier followed
+// by a byte sum and one fp16 fused multiply-add (TensorFold PR #740,
+// "Arithmetic" step 2).  The half mask/xor put each 16-bit half in +-[2^-3, 2),
+// so every state decodes finite (cuda-exl3 README, "Loading into a dim vLLM
+// has padded": all 65,536 codes decode finite).
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMcgMult = 0xCBAC1FEDu;
+constexpr uint32_t k3instMult = 0xCBAC1FEDu;
+constexpr uint32_t k3instAdd = 1u;
+constexpr uint32_t kMul1Mult = 0xCBAC1FEDu;
+constexpr uint32_t kHalfMask = 0x8FFF8FFFu;
+constexpr uint32_t kHalfXor = 0x30003000u;
+// fp16 bit patterns of the mul1 coefficients: 0x1EEE = 1774 * 2^-18 (nearest
+// fp16 to 1/147.8) and 0xC2E7 = -1767 * 2^-9 (nearest fp16 to -510/147.8).
+constexpr uint32_t kMul1ScaleH2 = 0x1EEE1EEEu;
+constexpr uint32_t kMul1BiasH2 = 0xC2E7C2E7u;
+// 1024.0 in both fp16 lanes: 0x6400 + t is the fp16 number 1024 + t for t < 1024.
+constexpr uint32_t kH2_1024 = 0x64006400u;
+
+enum Codebook { CB_3INST = 0, CB_MCG = 1, CB_MUL1 = 2 };
+
+__device__ __forceinline__ uint32_t hadd2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t lop3_mask_xor(uint32_t u) {
+  return (u & kHalfMask) ^ kHalfXor;  // one LOP3
+}
+
+// Two states -> one half2 register {value(s0) in bits 0..15, value(s1) in bits 16..31}.
+template <int CB>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t s0, uint32_t s1) {
+  if constexpr (CB == CB_MUL1) {
+    const uint32_t u0 = s0 * kMul1Mult;
+    const uint32_t u1 = s1 * kMul1Mult;
+    // byte sums t0, t1 (0..1020), biased by the fp16 pattern of 1024.0
+    const uint32_t t0 = __dp4a(u0, 0x01010101u, 0x6400u);
+    const uint32_t t1 = __dp4a(u1, 0x01010101u, 0x6400u);
+    const uint32_t p = __byte_perm(t0, t1, 0x5410);  // {1024+t0, 1024+t1}, exact
+    const uint32_t t = hsub2_u32(p, kH2_1024);        // {t0, t1}, exact
+    return hfma2_u32(t, kMul1ScaleH2, kMul1BiasH2);   // one rounding each
+  } else {
+    uint32_t u0, u1;
+    if constexpr (CB == CB_3INST) {
+      u0 = s0 * k3instMult + k3instAdd;
+      u1 = s1 * k3instMult + k3instAdd;
+    } else {
+      u0 = s0 * kMcgMult;
+      u1 = s1 * kMcgMult;
+    }
+    u0 = lop3_mask_xor(u0);
+    u1 = lop3_mask_xor(u1);
+    // {u0.lo, u1.lo} + {u0.hi, u1.hi}: each lane sums the two halves of one state
+    const uint32_t lo = __byte_perm(u0, u1, 0x5410);
+    const uint32_t hi = __byte_perm(u0, u1, 0x7632);
+    return hadd2_u32(lo, hi);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Trellis windows.
+//
+// A tile is 16*BITS int16 words = 8*BITS 32-bit words forming one circular,
+// little-endian bit stream of 256*BITS bits.  Value v's 16-bit state is the 16
+// bits ending just before position (v+1)*BITS (cuda-exl3 README, "Where the time
+// goes": 58-bit window for 8 values at 6 bits, index wrap modulo the tile).
+// Lane l decodes values 8l..8l+7 (lane*8 alignment), i.e. the window of bits
+// [8*l*BITS + BITS - 16, 8*l*BITS + 8*BITS), at most three 32-bit words.
+// ---------------------------------------------------------------------------
+template <int BITS>
+struct LaneWindow {
+  static constexpr int kWords = 8 * BITS;            // 32-bit words per tile
+  static constexpr int kBytes = 32 * BITS;           // bytes per tile
+  static constexpr int kNeed = (BITS <= 4) ? 2 : 3;  // words a lane reads
+  int idx[3];  // word indices within the tile (already wrapped)
+  int off;     // bit offset of the window start within word idx[0]
+
+  __device__ __forceinline__ explicit LaneWindow(int lane) {
+    int s = 8 * lane * BITS + BITS - 16;
+    if (s < 0) s += 256 * BITS;
+    const int w = s >> 5;
+    off = s & 31;
+    idx[0] = w;
+    idx[1] = (w + 1) % kWords;
+    idx[2] = (w + 2) % kWords;
+  }
+};
+
+// Aligned window: bit j of (a2:a1:a0) is stream bit (window start + j).
+struct Aligned {
+  uint32_t a0, a1, a2;
+};
+
+template <int BITS>
+__device__ __forceinline__ Aligned align_window(uint32_t w0, uint32_t w1, uint32_t w2, int off) {
+  Aligned a;
+  a.a0 = __funnelshift_r(w0, w1, off);
+  a.a1 = __funnelshift_r(w1, w2, off);
+  a.a2 = (BITS >= 7) ? (w2 >> off) : 0u;
+  return a;
+}
+
+// State of the lane's J-th value (J = 0..7): bits [J*BITS, J*BITS+16) of the aligned window.
+template <int BITS, int J>
+__device__ __forceinline__ uint32_t window_state(const Aligned& a) {
+  constexpr int p = J * BITS;
+  if constexpr (p + 16 <= 32) {
+    return (a.a0 >> p) & 0xFFFFu;
+  } else if constexpr (p < 32) {
+    return __funnelshift_r(a.a0, a.a1, p) & 0xFFFFu;
+  } else if constexpr (p + 16 <= 64) {
+    return (a.a1 >> (p - 32)) & 0xFFFFu;
+  } else if constexpr (p < 64) {
+    return __funnelshift_r(a.a1, a.a2, p - 32) & 0xFFFFu;
+  } else {
+    return (a.a2 >> (p - 64)) & 0xFFFFu;
+  }
+}
+
+// The lane's 8 values as 4 half2 registers, in mma.m16n8k16 B-fragment order:
+// b[0] = {k=2q, 2q+1; n=g}, b[1] = {k=2q+8, 2q+9; n=g}, b[2], b[3] = same for n=g+8
+// (TensorFold PR #740, "Arithmetic" step 2: a tile's value order is that of the
+// B fragments of two mma.m16n8k16).
+template <int BITS, int CB>
+__device__ __forceinline__ void decode_lane(const Aligned& a, uint32_t b[4]) {
+  b[0] = decode_pair<CB>(window_state<BITS, 0>(a), window_state<BITS, 1>(a));
+  b[1] = decode_pair<CB>(window_state<BITS, 2>(a), window_state<BITS, 3>(a));
+  b[2] = decode_pair<CB>(window_state<BITS, 4>(a), window_state<BITS, 5>(a));
+  b[3] = decode_pair<CB>(window_state<BITS, 6>(a), window_state<BITS, 7>(a));
+}
+
+// Load the lane's window words of one tile (tile_words = first 32-bit word of the tile).
+template <int BITS>
+__device__ __forceinline__ Aligned load_lane_window(const uint32_t* tile_words, const LaneWindow<BITS>& lw) {
+  const uint32_t w0 = tile_words[lw.idx[0]];
+  const uint32_t w1 = tile_words[lw.idx[1]];
+  const uint32_t w2 = (LaneWindow<BITS>::kNeed == 3) ? tile_words[lw.idx[2]] : 0u;
+  return align_window<BITS>(w0, w1, w2, lw.off);
+}
+
+// ---------------------------------------------------------------------------
+// 128-point Hadamard butterfly over one row held as 4 consecutive values per
+// lane (lane l holds elements 4l..4l+3).  Stages run in the fixed order of
+// strides 1, 2, 4, ..., 64; each stage maps (a, b) -> (a + b, a - b) for the
+// pair at indices (i, i + stride), i.e. H[i][j] = (-1)^popcount(i & j).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void fwht128_warp(float v[4], int lane) {
+  float t0 = v[0] + v[1], t1 = v[0] - v[1];
+  float t2 = v[2] + v[3], t3 = v[2] - v[3];
+  v[0] = t0 + t2;
+  v[2] = t0 - t2;
+  v[1] = t1 + t3;
+  v[3] = t1 - t3;
+#pragma unroll
+  for (int s = 1; s < 32; s <<= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[i], s);
+      v[i] = upper ? (p - v[i]) : (v[i] + p);
+    }
+  }
+}
+
+__device__ __forceinline__ uint16_t f32_to_out(float v, bool bf16) {
+  if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  return __half_as_ushort(__float2half_rn(v));
+}
+
+}  // namespace exl3

@@ -1,0 +1,139 @@
+// exl3_kernels_misc.cu -- width dispatch of the GEMM, the split-k epilogue and
+// the test-only decode kernels.
+#include "exl3_device.cuh"
+#include "exl3_launch.h"
+
+namespace exl3 {
+
+cudaError_t launch_gemm_mma(const GemmArgs& args, int bits, int cb, cudaStream_t stream) {
+  switch (bits) {
+    case 1: return launch_gemm_mma_bits<1>(args, cb, stream);
+    case 2: return launch_gemm_mma_bits<2>(args, cb, stream);
+    case 3: return launch_gemm_mma_bits<3>(args, cb, stream);
+    case 4: return launch_gemm_mma_bits<4>(args, cb, stream);
+    case 5: return launch_gemm_mma_bits<5>(args, cb, stream);
+    case 6: return launch_gemm_mma_bits<6>(args, cb, stream);
+    case 7: return launch_gemm_mma_bits<7>(args, cb, stream);
+    default: return launch_gemm_mma_bits<8>(args, cb, stream);
+  }
+}
+
+// Split-k epilogue (cuda-exl3 README, "One op per layer": the epilogue Hadamard
+// consumes the fp32 partials and re-zeroes the buffer; TensorFold PR #740: parts
+// are added in part order).  One warp per (row, 128-column block); lane l owns
+// columns 4l..4l+3 of the block: z = ((p0 + p1) + p2) + ..., then the same
+// butterfly, scale and rounding as the fused epilogue, then zeros written back.
+__global__ void __launch_bounds__(256) splitk_epilogue_kernel(const GemmArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t cb = a.n >> 7;
+  const int64_t units = a.m * cb;
+  const int64_t plane = a.m * a.n;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const bool bf16 = a.y_bf16 != 0;
+  uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps_total) {
+    const int64_t r = u / cb;
+    const int64_t col = (u - r * cb) * 128 + 4 * lane;
+    float* p = a.acc + r * a.n + col;
+    float4 s = *reinterpret_cast<const float4*>(p);
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int part = 1; part < a.parts; ++part) {
+      float* q = p + part * plane;
+      const float4 t = *reinterpret_cast<const float4*>(q);
+      s.x = s.x + t.x;
+      s.y = s.y + t.y;
+      s.z = s.z + t.z;
+      s.w = s.w + t.w;
+      *reinterpret_cast<float4*>(q) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float v[4] = {s.x, s.y, s.z, s.w};
+    fwht128_warp(v, lane);
+    const uint2 sv = *reinterpret_cast<const uint2*>(a.svh + col);
+    const float svf[4] = {__half2float(__ushort_as_half((uint16_t)(sv.x & 0xFFFF))),
+                          __half2float(__ushort_as_half((uint16_t)(sv.x >> 16))),
+                          __half2float(__ushort_as_half((uint16_t)(sv.y & 0xFFFF))),
+                          __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)))};
+    uint16_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = f32_to_out((v[i] * 0.125f) * svf[i], bf16);
+    uint2 w;
+    w.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+    w.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+    *reinterpret_cast<uint2*>(y + r * a.n + col) = w;
+  }
+}
+
+cudaError_t launch_splitk_epilogue(const GemmArgs& a, cudaStream_t stream) {
+  const int64_t units = a.m * (a.n >> 7);
+  const int64_t want = (units + 7) / 8;
+  const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  splitk_epilogue_kernel<<<blocks, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Test-only kernels: the same device decode as the GEMM, written out densely.
+// ---------------------------------------------------------------------------
+template <int CB>
+__global__ void test_codebook_kernel(uint16_t* out) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;  // states 2t, 2t+1
+  if (t < 32768) reinterpret_cast<uint32_t*>(out)[t] = decode_pair<CB>(2u * t, 2u * t + 1u);
+}
+
+cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream) {
+  if (cb == CB_3INST) test_codebook_kernel<CB_3INST><<<128, 256, 0, stream>>>(out);
+  else if (cb == CB_MCG) test_codebook_kernel<CB_MCG><<<128, 256, 0, stream>>>(out);
+  else test_codebook_kernel<CB_MUL1><<<128, 256, 0, stream>>>(out);
+  return cudaGetLastError();
+}
+
+// One warp per tile; lane l writes its 8 values at their (k, n) positions.
+template <int BITS, int CB>
+__global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t k, int64_t n, uint16_t* wq) {
+  const int lane = threadIdx.x & 31;
+  const int64_t NT = n >> 4;
+  const int64_t tiles = (k >> 4) * NT;
+  const int64_t tile = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (tile >= tiles) return;
+  const int64_t kt = tile / NT, nt = tile - kt * NT;
+  const LaneWindow<BITS> lw(lane);
+  const uint32_t* tw = reinterpret_cast<const uint32_t*>(trellis) + tile * (8 * BITS);
+  const Aligned al = load_lane_window<BITS>(tw, lw);
+  uint32_t b[4];
+  decode_lane<BITS, CB>(al, b);
+  const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int64_t kk = kt * 16 + 2 * q + ((r & 1) ? 8 : 0);
+    const int64_t nn = nt * 16 + g + ((r & 2) ? 8 : 0);
+    wq[kk * n + nn] = (uint16_t)(b[r] & 0xFFFF);
+    wq[(kk + 1) * n + nn] = (uint16_t)(b[r] >> 16);
+  }
+}
+
+template <int BITS>
+static cudaError_t launch_unpack_bits(const int16_t* t, int cb, int64_t k, int64_t n, uint16_t* wq,
+                                      cudaStream_t stream) {
+  const int64_t tiles = (k >> 4) * (n >> 4);
+  const unsigned blocks = (unsigned)((tiles + 7) / 8);
+  if (cb == CB_3INST) test_unpack_kernel<BITS, CB_3INST><<<blocks, 256, 0, stream>>>(t, k, n, wq);
+  else if (cb == CB_MCG) test_unpack_kernel<BITS, CB_MCG><<<blocks, 256, 0, stream>>>(t, k, n, wq);
+  else test_unpack_kernel<BITS, CB_MUL1><<<blocks, 256, 0, stream>>>(t, k, n, wq);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_test_unpack(const int16_t* trellis, int bits, int cb, int64_t k, int64_t n, uint16_t* wq,
+                               cudaStream_t stream) {
+  switch (bits) {
+    case 1: return launch_unpack_bits<1>(trellis, cb, k, n, wq, stream);
+    case 2: return launch_unpack_bits<2>(trellis, cb, k, n, wq, stream);
+    case 3: return launch_unpack_bits<3>(trellis, cb, k, n, wq, stream);
+    case 4: return launch_unpack_bits<4>(trellis, cb, k, n, wq, stream);
+    case 5: return launch_unpack_bits<5>(trellis, cb, k, n, wq, stream);
+    case 6: return launch_unpack_bits<6>(trellis, cb, k, n, wq, stream);
+    case 7: return launch_unpack_bits<7>(trellis, cb, k, n, wq, stream);
+    default: return launch_unpack_bits<8>(trellis, cb, k, n, wq, stream);
+  }
+}
+
+}  // namespace exl3

@@ -1,0 +1,42 @@
+// exl3_launch.h -- internal host-side launchers (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace exl3 {
+
+constexpr int kMaxShards = 8;
+
+// Everything one GEMM launch needs; passed by value as a kernel parameter.
+struct GemmArgs {
+  const uint16_t* xh;      // fp16 [S][m][k]
+  const int16_t* trellis;  // int16 [k/16][n/16][16*bits]
+  const uint16_t* svh;     // fp16 [n]
+  void* y;                 // [m][n], bf16 or fp16
+  float* acc;              // split-k workspace fp32 [P][m][n], or nullptr
+  int64_t m, k, n;
+  int32_t shard_cols[kMaxShards + 1];
+  int32_t num_shards;
+  int32_t parts;  // P (1 = no split)
+  int32_t y_bf16;
+};
+
+cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
+                                   int num_shards, uint16_t* xh, cudaStream_t stream);
+
+// mma.sync GEMM mainloop; with args.parts > 1 it writes fp32 partials to args.acc.
+cudaError_t launch_gemm_mma(const GemmArgs& args, int bits, int cb, cudaStream_t stream);
+
+// Sum the P partials in part order, rotate, scale, store y, zero the workspace.
+cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
+
+cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream);
+cudaError_t launch_test_unpack(const int16_t* trellis, int bits, int cb, int64_t k, int64_t n, uint16_t* wq,
+                               cudaStream_t stream);
+
+// Per-width instantiations of the mma.sync GEMM (one translation unit per width).
+template <int BITS>
+cudaError_t launch_gemm_mma_bits(const GemmArgs& args, int cb, cudaStream_t stream);
+
+}  // namespace exl3

@@ -55,8 +55,8 @@ def random_trellis(k: int, n: int, bits: int, g: torch.Generator) -> torch.Tenso
     """Uniform random int16 words, every bit pattern equally likely."""
     if k % 16 or n % 16:
         raise ValueError("k and n must be multiples of 16")
-    words = torch.randint(0, 1 << 16, (k // 16, n // 16, 16 * bits), generator=g, dtype=torch.int64)
-    return (words - (1 << 16) * (words >= (1 << 15))).to(torch.int16)
+    words = torch.randint(-(1 << 15), 1 << 15, (k // 16, n // 16, 16 * bits), generator=g, dtype=torch.int32)
+    return words.to(torch.int16)
 
 
 def make_layer(k: int, shard_widths: Sequence[int], bits: int, codebook: int, seed: int) -> Layer:
@@ -80,5 +80,4 @@ def make_x(m: int, k: int, seed: int) -> torch.Tensor:
 def random_words(count: int, seed: int) -> torch.Tensor:
     """Uniform int16 words (used for tile-level unpack tests)."""
     g = torch.Generator().manual_seed(seed)
-    w = torch.randint(0, 1 << 16, (count,), generator=g, dtype=torch.int64)
-    return (w - (1 << 16) * (w >= (1 << 15))).to(torch.int16)
+    return torch.randint(-(1 << 15), 1 << 15, (count,), generator=g, dtype=torch.int32).to(torch.int16)

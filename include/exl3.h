@@ -1,0 +1,151 @@
+/*
+ * exl3.h -- C ABI of libexl3.so, the EXL3 trellis-quantized linear layer on sm_103a.
+ *
+ * The layer computes
+ *
+ *     y = svh * H_N( Wq^T-contraction( H_K(x * suh) * 2^-4 ) ) * 2^-3
+ *
+ * where H_K / H_N are block-diagonal 128-point Hadamard transforms and Wq is
+ * decoded on the fly from 16x16 trellis tiles (cuda-exl3 README, "Why custom
+ * kernels" and "One op per layer"; TensorFold PR #740, "Arithmetic").
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, C-contiguous,
+ *    16-byte aligned.  The library allocates nothing and keeps no per-layer
+ *    state; it never synchronises the host.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Work is enqueued asynchronously on it.
+ *  - Every argument is validated on the host before anything is launched.  An
+ *    invalid call returns EXL3_EINVAL (or EXL3_EWORKSPACE) and launches nothing.
+ *    A launch failure returns EXL3_ECUDA; exl3_last_error() gives the CUDA text.
+ *  - fp16 / bf16 values are passed as their 16-bit patterns (uint16_t).
+ *  - m == 0 is an empty batch: the call returns EXL3_OK and launches nothing;
+ *    the activation, output and workspace pointers may then be NULL.
+ *    m may be at most EXL3_MAX_ROWS.
+ *  - k and n are multiples of 128 (whole Hadamard blocks; cuda-exl3 README,
+ *    "Loading into a dim vLLM has padded").  bits is 1..8 (cuda-exl3 README,
+ *    "What is supported").
+ */
+#ifndef EXL3_H
+#define EXL3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { EXL3_CB_3INST = 0, EXL3_CB_MCG = 1, EXL3_CB_MUL1 = 2 } exl3_codebook_t;
+typedef enum { EXL3_F16 = 0, EXL3_BF16 = 1 } exl3_dtype_t;
+typedef enum {
+  EXL3_OK = 0,
+  EXL3_EINVAL = 1,       /* bad shape, pointer, alignment, width, codebook or shard map */
+  EXL3_EUNSUPPORTED = 2, /* valid request this build does not implement */
+  EXL3_EWORKSPACE = 3,   /* split-k accumulator too small */
+  EXL3_ECUDA = 4         /* a CUDA launch or runtime call failed */
+} exl3_status_t;
+
+/* Largest batch (rows of x) one call accepts. */
+#define EXL3_MAX_ROWS (1 << 22)
+
+/* Maximum number of fused shards in one call (qkv = 3, gate_up = 2). */
+#define EXL3_MAX_SHARDS 8
+
+/*
+ * exl3_input_transform -- input rotation of every shard in one pass over x.
+ *
+ * TensorFold PR #740, "Arithmetic" step 1; cuda-exl3 README, "One op per layer"
+ * (activation transform fused, bf16 -> fp16 folded into the load).  For each
+ * shard s, row r and 128-block b of k:
+ *     xh[s][r][128b+i] = fp16_rne( 2^-4 * sum_j H[i][j] * (x[r][128b+j] * suh[s][128b+j]) )
+ * with H[i][j] = (-1)^popcount(i & j), the product x*suh exact in fp32 and the
+ * sum taken as a radix-2 butterfly in fp32 with a fixed order of adds.
+ *
+ *   x        device, [m][k] of x_dtype (bf16 or fp16)
+ *   suh      device, fp16 [num_shards][k]
+ *   xh       device, fp16 [num_shards][m][k] (output)
+ */
+exl3_status_t exl3_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t m, int64_t k,
+                                   const uint16_t* suh, int32_t num_shards, uint16_t* xh,
+                                   void* stream);
+
+/*
+ * exl3_gemm -- trellis decode fused into the contraction, output rotation fused
+ * into the epilogue, all shards of a fused layer in one launch.
+ *
+ * cuda-exl3 README, "Why custom kernels" (a block owns its columns and the whole
+ * k extent, so the output Hadamard and svh fold into the epilogue) and "Notes on
+ * the format" (trellis and svh concatenate along n; one suh row, hence one xh
+ * slice, per shard).  TensorFold PR #740, "Arithmetic" steps 2-3.
+ *     z[r][c]  = sum_k xh[s(c)][r][k] * Wq[k][c]      (fp16 products, fp32 sums)
+ *     y[r][c]  = out_rne( svh[c] * 2^-3 * sum_j H[i][j] z[r][128b+j] ),  c = 128b+i
+ * Wq[k][c] is decoded from trellis tile (k/16, c/16).  The fp32 sum over k runs
+ * in a fixed order that does not depend on m, so each row's bytes are the same
+ * at every batch size.
+ *
+ *   xh         device, fp16 [num_shards][m][k] (exl3_input_transform's output)
+ *   trellis    device, int16 [k/16][n/16][16*bits]
+ *   bits       1..8;  cb: codebook id
+ *   svh        device, fp16 [n]
+ *   shard_cols HOST, int32 [num_shards+1]: 0 = c_0 < c_1 < ... < c_S = n, multiples
+ *              of 128; shard s owns output columns [c_s, c_{s+1})
+ *   y          device, [m][n] of y_dtype (output)
+ */
+exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis,
+                        int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
+                        const int32_t* shard_cols, int32_t num_shards, void* y,
+                        exl3_dtype_t y_dtype, int64_t n, void* stream);
+
+/*
+ * Split-k variant.  cuda-exl3 README, "One op per layer" (split-k for narrow
+ * layers: partials into an fp32 accumulator, an epilogue kernel does the
+ * Hadamard and re-zeroes the buffer); TensorFold PR #740, "Arithmetic" (k
+ * blocks split into a number of parts fixed by the shape, parts added in part
+ * order).  Part p covers a contiguous range of whole 128-row blocks of k; its
+ * fp32 partial goes to acc[p][r][c]; the epilogue sums p = 0..P-1 in order,
+ * applies the output rotation, writes y and writes zeros back to acc.
+ *
+ * exl3_splitk_parts(k, n) is the number of parts P; it depends on the shape only
+ * (never on m), so rows stay byte-equal across batch sizes.  It is a pure host
+ * function.  exl3_splitk_workspace_bytes(m, k, n) = P * m * n * 4.
+ *
+ *   acc        device, fp32 [P][m][n].  Must be all zero on entry; it is all zero
+ *              again when the call's work completes.  Calls that share one acc
+ *              must be ordered on one stream.
+ *   acc_bytes  size of acc in bytes; smaller than the workspace size -> EXL3_EWORKSPACE
+ *   other arguments as exl3_gemm.
+ */
+int32_t exl3_splitk_parts(int64_t k, int64_t n);
+size_t exl3_splitk_workspace_bytes(int64_t m, int64_t k, int64_t n);
+exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis,
+                               int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
+                               const int32_t* shard_cols, int32_t num_shards, void* y,
+                               exl3_dtype_t y_dtype, int64_t n, float* acc, size_t acc_bytes,
+                               void* stream);
+
+/*
+ * Test-only entry points (they run the same device decode as exl3_gemm).
+ *
+ * exl3_test_codebook: out[s] = fp16 bits of codebook cb at state s, s = 0..65535
+ *   (TensorFold PR #740, "Tests": all 65,536 states of each codebook).
+ *   out: device, uint16 [65536].
+ * exl3_test_unpack: wq[k][n] = decoded weights of the whole trellis as fp16 bits
+ *   (TensorFold PR #740, "Tests": random tiles at every width and codebook).
+ *   trellis: device int16 [k/16][n/16][16*bits]; wq: device uint16 [k][n].
+ *   k and n need only be multiples of 16 here.
+ */
+exl3_status_t exl3_test_codebook(exl3_codebook_t cb, uint16_t* out, void* stream);
+exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
+                               int64_t k, int64_t n, uint16_t* wq, void* stream);
+
+/* Static text for a status code. */
+const char* exl3_status_string(exl3_status_t status);
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char* exl3_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXL3_H */

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Bars (from the layer's specification):
+  * codebook values and unpacked Wq: bit-exact;
+  * input rotation: within one fp16 rounding of the exact value plus the fp32
+    butterfly's rounding bound;
+  * linear output: |y_gpu - y_oracle| <= 4e-3 * max_r |y_oracle[r, c]| per column,
+    the max taken over the rows of the largest batch of the case;
+  * every row byte-equal at every batch size; a fused multi-shard launch
+    byte-equal to separate launches; the split-k workspace zero after a call.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exl3_trellis_quantized_gb300 as E
+from exl3_trellis_quantized_gb300 import synthetic
+from oracle import exl3_oracle as O
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+TOL = 4e-3
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy()
+
+
+def _bits(t):
+    return t.detach().cpu().numpy().view(np.uint16)
+
+
+def _dev(layer):
+    return (layer.trellis.to(DEV), layer.suh.to(DEV), layer.svh.to(DEV))
+
+
+def _oracle(x, layer, col_blocks=None):
+    return O.linear(_np(x), layer.trellis.numpy(), layer.bits, layer.codebook, _np(layer.suh), _np(layer.svh),
+                    layer.shard_cols, col_blocks=col_blocks)
+
+
+def _assert_columns(got, ref, what=""):
+    colmax = np.abs(ref).max(axis=0)
+    err = np.abs(got - ref)
+    bad = err > TOL * colmax
+    assert not bad.any(), f"{what}: {bad.sum()} values out of tolerance, worst err/colmax {np.max(err / colmax):.3e}"
+    return float(np.max(err / colmax))
+
+
+def _run(layer, x, out_dtype, split, m=None):
+    tr, suh, svh = _dev(layer)
+    xd = x.to(DEV) if m is None else x[:m].to(DEV)
+    acc = None
+    if split:
+        nbytes = E.splitk_workspace_bytes(xd.shape[0], layer.k, layer.n)
+        acc = torch.zeros(max(1, nbytes // 4), dtype=torch.float32, device=DEV)
+    y = E.linear(xd, tr, layer.bits, layer.codebook, suh, svh, layer.shard_cols, out_dtype=out_dtype, acc=acc)
+    torch.cuda.synchronize()
+    return y, acc
+
+
+# ---------------------------------------------------------------------------
+# decode primitives
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_codebook_all_states_bit_exact(cb):
+    got = _bits(E.binding.test_codebook(cb, DEV))
+    want = O.codebook(cb, np.arange(65536))
+    assert np.array_equal(got, want), f"{np.sum(got != want)} states differ"
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_unpack_bit_exact(bits, cb):
+    g = torch.Generator().manual_seed(40 + 3 * bits + cb)
+    tr = synthetic.random_trellis(64, 96, bits, g)
+    got = _bits(E.binding.test_unpack(tr.to(DEV), bits, cb))
+    want = O.f64_to_half_bits(O.dequantize(tr.numpy(), bits, cb))
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------------------
+# input rotation
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
+def test_input_transform_parity(xdtype):
+    m, k, s = 37, 640, 3
+    layer = synthetic.make_layer(k, [128] * s, 4, 1, seed=5)
+    x = synthetic.make_x(m, k, seed=5).to(xdtype)
+    xh = E.input_transform(x.to(DEV), layer.suh.to(DEV))
+    torch.cuda.synchronize()
+    got = _np(xh)
+    ref = O.input_transform(_np(x), _np(layer.suh))
+    # fp32 butterfly: 7 rounded add stages over 128 exact products
+    xs = np.abs(_np(x))[None] * np.abs(_np(layer.suh))[:, None, :]
+    blk_sum = np.repeat(xs.reshape(s, m, k // 128, 128).sum(-1), 128, axis=-1)
+    e = 8 * 2.0 ** -24 * blk_sum * 2.0 ** -4
+    # rounding to fp16 is monotonic: the result lies between the roundings of ref -+ e
+    lo = (ref - e).astype(np.float16).astype(np.float64)
+    hi = (ref + e).astype(np.float16).astype(np.float64)
+    bad = (got < lo) | (got > hi)
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{bad.sum()} bad; first {tuple(i)}: got {got[tuple(i)]!r} ref {ref[tuple(i)]!r} "
+                             f"lo {lo[tuple(i)]!r} hi {hi[tuple(i)]!r}")
+
+
+# ---------------------------------------------------------------------------
+# the layer: coverage of widths x codebooks, batch sizes, dtypes
+# ---------------------------------------------------------------------------
+
+M_SET = [1, 2, 7, 16, 64, 300]
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_linear_coverage_small_split(bits, cb):
+    """K=1024, N=512 (under 96 column blocks, exercising split-k), all rows checked."""
+    k, n = 1024, 512
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=1001 + 10 * bits + cb)
+    x = synthetic.make_x(300, k, seed=1001)
+    out_dtype = torch.float16 if (bits + cb) % 2 else torch.bfloat16
+    ref = _oracle(x, layer)
+    for split in (False, True):
+        y, acc = _run(layer, x, out_dtype, split)
+        _assert_columns(_np(y), ref, f"split={split}")
+        if split:
+            assert not acc.any(), "split-k workspace not re-zeroed"
+        for m in M_SET[:-1]:
+            ym, _ = _run(layer, x, out_dtype, split, m=m)
+            assert torch.equal(ym.view(torch.int16), y[:m].view(torch.int16)), f"row bytes differ at m={m}"
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_linear_coverage_2048(bits, cb):
+    """K=2048, N=2048; three sampled column blocks checked against the oracle."""
+    k, n = 2048, 2048
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=1001 + 10 * bits + cb + 5)
+    x = synthetic.make_x(300, k, seed=1002)
+    out_dtype = torch.bfloat16 if (bits + cb) % 2 else torch.float16
+    blocks = [0, 7, 15]
+    ref = _oracle(x, layer, blocks)
+    y, _ = _run(layer, x, out_dtype, False)
+    got = _np(y).reshape(300, 16, 128)[:, blocks].reshape(300, -1)
+    _assert_columns(got, ref)
+    for m in (1, 16, 64):
+        ym, _ = _run(layer, x, out_dtype, False, m=m)
+        assert torch.equal(ym.view(torch.int16), y[:m].view(torch.int16))
+
+
+def test_fused_shards_equal_separate_launches():
+    k, bits, cb = 512, 5, 2
+    layer = synthetic.make_layer(k, [256, 128, 384], bits, cb, seed=77)
+    x = synthetic.make_x(20, k, seed=77)
+    y, _ = _run(layer, x, torch.bfloat16, False)
+    tr, suh, svh = _dev(layer)
+    xd = x.to(DEV)
+    for s in range(3):
+        a, b = layer.shard_cols[s], layer.shard_cols[s + 1]
+        ys = E.linear(xd, tr[:, a // 16:b // 16].contiguous(), bits, cb, suh[s:s + 1].contiguous(),
+                      svh[a:b].contiguous(), [0, b - a])
+        torch.cuda.synchronize()
+        assert torch.equal(ys.view(torch.int16), y[:, a:b].view(torch.int16)), s
+    _assert_columns(_np(y), _oracle(x, layer))
+
+
+def test_splitk_workspace_reused_across_calls():
+    """One workspace, several calls on one stream: zero after each, results stable."""
+    k, n, bits, cb = 1024, 512, 3, 1
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=88)
+    x = synthetic.make_x(33, k, seed=88).to(DEV)
+    tr, suh, svh = _dev(layer)
+    acc = torch.zeros(E.splitk_workspace_bytes(33, k, n) // 4, dtype=torch.float32, device=DEV)
+    ys = [E.linear(x, tr, bits, cb, suh, svh, layer.shard_cols, acc=acc) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert not acc.any()
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    assert torch.equal(ys[0].view(torch.int16), ys[2].view(torch.int16))
+
+
+def test_empty_batch():
+    layer = synthetic.make_layer(256, [256], 4, 1, seed=3)
+    tr, suh, svh = _dev(layer)
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device=DEV)
+    y = E.linear(x, tr, 4, 1, suh, svh, layer.shard_cols)
+    assert y.shape == (0, 256)
+
+
+# ---------------------------------------------------------------------------
+# full-size layers, in the launch configuration the benchmark times; every row
+# of sampled 128-column blocks is checked against the oracle
+# ---------------------------------------------------------------------------
+
+FULL = [
+    # name, k, shard widths, bits, codebook, m, split
+    ("single_2048x4096_4b_mcg", 2048, [4096], 4, 1, 16, False),
+    ("q_proj_5120x12288_6b_mcg", 5120, [12288], 6, 1, 4096, False),
+    ("gate_up_5120x2x17408_5b_mul1", 5120, [17408, 17408], 5, 2, 512, False),
+    ("down_17408x5120_6b_mul1_splitk", 17408, [5120], 6, 2, 512, True),
+    ("lm_head_4096x154880_6b_3inst", 4096, [154880], 6, 0, 16, False),
+    ("proj_12288x4096_5b_mcg", 12288, [4096], 5, 1, 2048, False),
+]
+
+
+@pytest.mark.parametrize("name,k,widths,bits,cb,m,split", FULL, ids=[f[0] for f in FULL])
+def test_full_size_sampled(name, k, widths, bits, cb, m, split):
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=2000 + len(name))
+    x = synthetic.make_x(m, k, seed=2000)
+    y, acc = _run(layer, x, torch.bfloat16, split)
+    rows = list(range(m))  # the column max of the tolerance is over every row of the batch
+    nb = layer.n // 128
+    blocks = sorted({0, nb // 2, nb - 1})
+    for s in range(1, len(widths)):  # first block of every further shard
+        blocks.append(layer.shard_cols[s] // 128)
+    blocks = sorted(set(blocks))
+    ref = _oracle(x[rows], layer, blocks)
+    got = _np(y)[rows].reshape(len(rows), nb, 128)[:, blocks].reshape(len(rows), -1)
+    _assert_columns(got, ref, name)
+    assert not torch.isnan(y.float()).any()
+    if split:
+        assert not acc.any()
