@@ -8,6 +8,7 @@ PyTorch fallback; if the library is missing every call raises.
 from .binding import (  # noqa: F401
     CODEBOOKS,
     Exl3Error,
+    device_status,
     gemm,
     gemm_splitk,
     input_transform,

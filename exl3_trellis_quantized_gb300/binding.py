@@ -53,12 +53,21 @@ def lib() -> ctypes.CDLL:
     L.exl3_test_unpack.argtypes = [vp, i32, ctypes.c_int, i64, i64, vp, vp]
     L.exl3_status_string.argtypes = [ctypes.c_int]
     L.exl3_status_string.restype = ctypes.c_char_p
+    L.exl3_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.exl3_device_status.restype = ctypes.c_int
     L.exl3_last_error.argtypes = []
     L.exl3_last_error.restype = ctypes.c_char_p
     for name in ("exl3_input_transform", "exl3_gemm", "exl3_gemm_splitk", "exl3_test_codebook", "exl3_test_unpack"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
+
+
+def device_status() -> int:
+    """Read and clear the kernels' device-side error flags (synchronises the device)."""
+    flags = ctypes.c_uint32(0)
+    _check(lib().exl3_device_status(ctypes.byref(flags)), "exl3_device_status")
+    return int(flags.value)
 
 
 def status_string(status: int) -> str:

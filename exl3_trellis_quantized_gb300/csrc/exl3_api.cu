@@ -89,7 +89,7 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
   exl3_status_t st = check_gemm(xh, m, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
   if (st != EXL3_OK) return st;
   if (m == 0) return EXL3_OK;
-  return cuda_status(exl3::launch_gemm_mma(a, bits, cb, static_cast<cudaStream_t>(stream)), "exl3_gemm");
+  return cuda_status(exl3::launch_gemm_tc(a, bits, cb, static_cast<cudaStream_t>(stream)), "exl3_gemm");
 }
 
 // Shape-only split policy: the number of parts P makes (n/128) * P work units
@@ -138,7 +138,7 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.parts == 1) {
     // one part: the fused epilogue already does everything; acc stays zero
-    return cuda_status(exl3::launch_gemm_mma(a, bits, cb, s), "exl3_gemm_splitk");
+    return cuda_status(exl3::launch_gemm_tc(a, bits, cb, s), "exl3_gemm_splitk");
   }
   st = cuda_status(exl3::launch_gemm_mma(a, bits, cb, s), "exl3_gemm_splitk parts");
   if (st != EXL3_OK) return st;
@@ -171,5 +171,10 @@ const char* exl3_status_string(exl3_status_t status) {
 }
 
 const char* exl3_last_error(void) { return g_last_error; }
+
+exl3_status_t exl3_device_status(uint32_t* flags) {
+  if (flags == nullptr) return EXL3_EINVAL;
+  return cuda_status(exl3::take_device_errors(flags), "exl3_device_status");
+}
 
 }  // extern "C"

@@ -1,0 +1,280 @@
+// exl3_gemm_tc.cuh -- EXL3 GEMM on the 5th-generation tensor cores (tcgen05).
+//
+// One CTA owns BN output columns (BN/128 output Hadamard blocks) and RG*128
+// rows over the whole k extent (cuda-exl3 README, "Why custom kernels": a block
+// owns BM rows x BN columns and the whole k, reads its trellis slice once and
+// folds the output Hadamard and svh into the epilogue).  Warp roles:
+//
+//   warp 0      TMA producer: per 64-wide k stage, four 1-D bulk copies of the
+//               stage's trellis tile rows and RG tiled copies of the rotated
+//               activations xh (128-byte swizzle), all completing on full[s];
+//   warp 1      TMEM allocator and MMA issuer: one thread issues
+//               tcgen05.mma kind::f16 (M=128, N=BN, K=16) per row group and
+//               16-wide k step into the fp32 accumulators in tensor memory;
+//   warps 2..9  decoders: each lane decodes its 8 values of a 16x16 tile
+//               (bitshift trellis + procedural codebook, TensorFold PR #740,
+//               "Arithmetic" step 2) into registers in mma B-fragment order and
+//               stmatrix writes them into the swizzled K-major B operand; then
+//               the epilogue: tcgen05.ld of a row's 128 accumulators, the
+//               128-point butterfly in registers, *2^-3 * svh, bf16/fp16 store.
+//
+// Each tile is decoded exactly once per CTA.  The fp32 sum over k is a fixed
+// sequence of tcgen05 k16 steps in ascending k for every row, whatever m is, so
+// rows are byte-equal across batch sizes.  Every wait is bounded: a kernel that
+// gives up records kErrWaitTimeout and skips its stores.
+#pragma once
+
+#include "exl3_device.cuh"
+#include "exl3_launch.h"
+#include "exl3_sm100.cuh"
+
+namespace exl3 {
+
+constexpr int kTcDecodeWarps = 8;   // decoder / epilogue warps
+constexpr int kTcThreads = 32 * (2 + kTcDecodeWarps);
+constexpr int kTcSmemBudget = 227 * 1024;
+
+template <int BITS, int BN, int RG>
+struct TcCfg {
+  static constexpr int kXBytes = 128 * 128;                 // one row group of xh per stage (16 KB)
+  static constexpr int kWBytes = BN * 128;                  // decoded B operand per stage
+  static constexpr int kTrRowBytes = (BN / 16) * 32 * BITS;  // one k16 row of BN/16 tiles
+  static constexpr int kTrBytes = 4 * kTrRowBytes;          // four k16 rows per stage
+  static constexpr int kStageBytes = RG * kXBytes + kWBytes + kTrBytes;
+  static constexpr int kCtrlBytes = 1024;
+  static constexpr int kStages0 = (kTcSmemBudget - 1024 - kCtrlBytes) / kStageBytes;
+  static constexpr int kStages = kStages0 > 6 ? 6 : kStages0;
+  static constexpr int kSmem = 1024 + kCtrlBytes + kStages * kStageBytes;
+  static constexpr int kTmemCols = RG * BN <= 128 ? 128 : (RG * BN <= 256 ? 256 : 512);
+  static_assert(RG * BN <= 512, "accumulators exceed tensor memory");
+  static_assert(kStages >= 2, "not enough shared memory for two stages");
+};
+
+
+template <int BITS, int CB, int BN, int RG>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ TcParams p) {
+  using C = TcCfg<BITS, BN, RG>;
+  constexpr int ST = C::kStages;
+  constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
+  const GemmArgs& a = p.a;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(base);
+  uint64_t* wfull = full + ST;
+  uint64_t* empty = wfull + ST;
+  uint64_t* accfull = empty + ST;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
+  volatile uint32_t* failed = tmem_slot + 1;  // set by the MMA issuer if any wait gave up
+  uint8_t* stages = base + C::kCtrlBytes;
+  auto xs_stage = [&](int s) { return stages + s * C::kStageBytes; };
+  auto w_stage = [&](int s) { return stages + s * C::kStageBytes + RG * C::kXBytes; };
+  auto tr_stage = [&](int s) { return stages + s * C::kStageBytes + RG * C::kXBytes + C::kWBytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t c0 = (int64_t)blockIdx.x * BN;
+  const int64_t row0 = (int64_t)blockIdx.y * (128 * RG);
+  const int nk = (int)(a.k / kTcBK);
+
+  int shard = 0;
+#pragma unroll
+  for (int i = 1; i < kMaxShards; ++i)
+    if (i < a.num_shards && c0 >= a.shard_cols[i]) shard = i;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&wfull[s], kTcDecodeWarps);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accfull, 1);
+    *failed = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&xmap);
+      const int64_t NT = a.n >> 4;
+      const int64_t nt0 = c0 >> 4;
+      const uint32_t tx = 4u * C::kTrRowBytes + (uint32_t)RG * (uint32_t)p.box_rows * 128u;
+      for (int it = 0; it < nk; ++it) {
+        const int s = it % ST;
+        const uint32_t ph = (uint32_t)(it / ST) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u)) break;
+        mbar_arrive_expect_tx(&full[s], tx);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t kt = (int64_t)it * 4 + j;
+          const int16_t* src = a.trellis + (kt * NT + nt0) * (16 * BITS);
+          tma_bulk_g2s(tr_stage(s) + j * C::kTrRowBytes, src, C::kTrRowBytes, &full[s]);
+        }
+#pragma unroll
+        for (int r = 0; r < RG; ++r)
+          tma_tile3d_g2s(xs_stage(s) + r * C::kXBytes, &xmap, it * kTcBK, (int)(row0 + r * 128), shard, &full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      bool ok = true;
+      for (int it = 0; it < nk && ok; ++it) {
+        const int s = it % ST;
+        const uint32_t ph = (uint32_t)(it / ST) & 1u;
+        ok = mbar_wait(&full[s], ph) && mbar_wait(&wfull[s], ph);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t xa = smem_u32(xs_stage(s));
+        const uint32_t wa = smem_u32(w_stage(s));
+#pragma unroll
+        for (int j = 0; j < kTcBK / 16; ++j) {
+#pragma unroll
+          for (int r = 0; r < RG; ++r) {
+            tc_mma_f16(tmem + r * BN, sdesc_sw128(xa + r * C::kXBytes + j * 32), sdesc_sw128(wa + j * 32), kIdesc,
+                       (it | j) != 0);
+          }
+        }
+        tc_commit(&empty[s]);
+      }
+      if (!ok) *failed = 1u;
+      tc_commit(accfull);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- decoders ----------------
+    const int dw = warp - 2;
+    const LaneWindow<BITS> lw(lane);
+    const int row_in = (lane & 7) + ((lane >> 4) << 3);  // stmatrix row of this lane within a 16-row tile
+    const int chunk_hi = (lane >> 3) & 1;                // second 8-wide k half
+    constexpr int kTilesN = BN / 16;
+    for (int it = 0; it < nk; ++it) {
+      const int s = it % ST;
+      const uint32_t ph = (uint32_t)(it / ST) & 1u;
+      if (!mbar_wait(&full[s], ph)) break;
+      const uint32_t* trw = reinterpret_cast<const uint32_t*>(tr_stage(s));
+      const uint32_t wbase = smem_u32(w_stage(s));
+#pragma unroll
+      for (int t = dw; t < 4 * kTilesN; t += kTcDecodeWarps) {
+        const int kt_l = t / kTilesN;
+        const int nt_l = t - kt_l * kTilesN;
+        const Aligned al = load_lane_window<BITS>(trw + (kt_l * kTilesN + nt_l) * (8 * BITS), lw);
+        uint32_t b[4];
+        decode_lane<BITS, CB>(al, b);
+        const int row = nt_l * 16 + row_in;
+        const int chunk = 2 * kt_l + chunk_hi;
+        stmatrix_x4(wbase + row * 128 + ((chunk ^ (row & 7)) << 4), b[0], b[1], b[2], b[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wfull[s]);
+    }
+
+    // ---------------- epilogue ----------------
+    const bool ok = mbar_wait(accfull, 0) && *failed == 0u;
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const int grp = dw >> 2;
+    constexpr int kJobs = RG * (BN / 128);
+    const bool bf16 = a.y_bf16 != 0;
+    uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
+    for (int job = grp; job < kJobs; job += 2) {
+      __syncwarp();
+      const int r = job / (BN / 128);
+      const int hb = job - r * (BN / 128);
+      const int64_t row = row0 + r * 128 + quarter * 32 + lane;
+      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + hb * 128);
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t q[32];
+        tmem_ld_32x32b_x32(taddr + c * 32, q);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(q[i]);
+      }
+      if (!ok || row >= a.m) continue;  // after the warp-collective loads
+      // 128-point butterfly, strides 1, 2, ..., 64; (a, b) -> (a + b, a - b)
+#pragma unroll
+      for (int h = 1; h < 128; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          if ((i & h) == 0) {
+            const float x0 = v[i], x1 = v[i + h];
+            v[i] = x0 + x1;
+            v[i + h] = x0 - x1;
+          }
+        }
+      }
+      const int64_t col = c0 + hb * 128;
+      const uint4* sv = reinterpret_cast<const uint4*>(a.svh + col);
+      uint4* dst = reinterpret_cast<uint4*>(y + row * a.n + col);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint4 s8 = sv[c];
+        const uint32_t sw[4] = {s8.x, s8.y, s8.z, s8.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float s_lo = __half2float(__ushort_as_half((uint16_t)(sw[i] & 0xFFFF)));
+          const float s_hi = __half2float(__ushort_as_half((uint16_t)(sw[i] >> 16)));
+          const uint16_t lo = f32_to_out((v[c * 8 + 2 * i] * 0.125f) * s_lo, bf16);
+          const uint16_t hi = f32_to_out((v[c * 8 + 2 * i + 1] * 0.125f) * s_hi, bf16);
+          o[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+        }
+        dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int BITS, int CB, int BN, int RG>
+cudaError_t launch_tc_variant(const CUtensorMap& xmap, const TcParams& p, cudaStream_t stream) {
+  using C = TcCfg<BITS, BN, RG>;
+  auto kern = gemm_tc_kernel<BITS, CB, BN, RG>;
+  static bool configured = false;  // benign race: every thread sets the same attribute
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const dim3 grid((unsigned)(p.a.n / BN), (unsigned)((p.a.m + 128 * RG - 1) / (128 * RG)), 1);
+  kern<<<grid, kTcThreads, C::kSmem, stream>>>(xmap, p);
+  return cudaGetLastError();
+}
+
+template <int BITS, int CB>
+cudaError_t launch_tc_cb(const CUtensorMap& xmap, const TcParams& p, int bn, int rg, cudaStream_t stream) {
+  (void)bn;
+  (void)rg;
+  return launch_tc_variant<BITS, CB, 128, 1>(xmap, p, stream);
+}
+
+template <int BITS>
+cudaError_t launch_gemm_tc_bits(const CUtensorMap& xmap, const TcParams& p, int cb, int bn, int rg,
+                                cudaStream_t stream) {
+  switch (cb) {
+    case CB_3INST:
+      return launch_tc_cb<BITS, CB_3INST>(xmap, p, bn, rg, stream);
+    case CB_MCG:
+      return launch_tc_cb<BITS, CB_MCG>(xmap, p, bn, rg, stream);
+    default:
+      return launch_tc_cb<BITS, CB_MUL1>(xmap, p, bn, rg, stream);
+  }
+}
+
+}  // namespace exl3

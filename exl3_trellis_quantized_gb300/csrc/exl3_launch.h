@@ -1,6 +1,7 @@
 // exl3_launch.h -- internal host-side launchers (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,21 @@ cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
 cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream);
 cudaError_t launch_test_unpack(const int16_t* trellis, int bits, int cb, int64_t k, int64_t n, uint16_t* wq,
                                cudaStream_t stream);
+
+// tcgen05 GEMM (one translation unit per width); parts > 1 is not handled here.
+constexpr int kTcBK = 64;  // k per pipeline stage (one 128-byte swizzle row of fp16)
+struct TcParams {
+  GemmArgs a;
+  int32_t box_rows;  // rows per xh tile copy (<= 128)
+};
+cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream);
+template <int BITS>
+cudaError_t launch_gemm_tc_bits(const CUtensorMap& xmap, const TcParams& p, int cb, int bn, int rg,
+                                cudaStream_t stream);
+// Read and clear the wait-timeout flags of every kernel translation unit (synchronous).
+cudaError_t take_device_errors(uint32_t* flags);
+template <int BITS>
+cudaError_t take_device_error_tc(uint32_t* flags);
 
 // Per-width instantiations of the mma.sync GEMM (one translation unit per width).
 template <int BITS>

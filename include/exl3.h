@@ -139,6 +139,16 @@ exl3_status_t exl3_test_codebook(exl3_codebook_t cb, uint16_t* out, void* stream
 exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                int64_t k, int64_t n, uint16_t* wq, void* stream);
 
+/*
+ * exl3_device_status -- read and clear the library's device-side error flags.
+ * Every wait inside the kernels is bounded; a kernel that gives up sets bit 0
+ * (EXL3_DEVERR_WAIT_TIMEOUT) and skips its stores instead of hanging.  This call
+ * synchronises the current device (it is meant for tests and diagnostics).
+ *   flags: host pointer, receives the OR of all flags set since the last call.
+ */
+#define EXL3_DEVERR_WAIT_TIMEOUT 1u
+exl3_status_t exl3_device_status(uint32_t* flags);
+
 /* Static text for a status code. */
 const char* exl3_status_string(exl3_status_t status);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */

@@ -22,6 +22,13 @@ DEV = torch.device("cuda:0")
 TOL = 4e-3
 
 
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    """Every test must leave no wait-timeout flag behind."""
+    yield
+    assert E.device_status() == 0, "a kernel gave up on a bounded wait"
+
+
 def _np(t):
     return t.detach().float().cpu().numpy()
 
