@@ -63,6 +63,7 @@ exl3_status_t check_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t
   for (int i = 0; i <= num_shards; ++i) a->shard_cols[i] = shard_cols[i];
   a->parts = 1;
   a->y_bf16 = (y_dtype == EXL3_BF16) ? 1 : 0;
+  a->one = 1u;
   return EXL3_OK;
 }
 

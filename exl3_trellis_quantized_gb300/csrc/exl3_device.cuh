@@ -112,34 +112,59 @@ struct LaneWindow {
   }
 };
 
-// Aligned window: bit j of (a2:a1:a0) is stream bit (window start + j).
+// Multipliers the decoder uses for shifts it runs on the integer multiply-add
+// pipe.  They are derived at run time from a kernel argument equal to 1 so the
+// compiler keeps them as multiplies (the ALU pipe that executes shifts, masks
+// and permutes is the decoder's bottleneck; IMAD runs on a separate pipe).
+struct MulConsts {
+  uint32_t pow2[17];  // pow2[i] = 1 << i
+  __device__ __forceinline__ explicit MulConsts(uint32_t one) {
+#pragma unroll
+    for (int i = 0; i <= 16; ++i) pow2[i] = one << i;
+  }
+};
+
+// Aligned views of a lane's window: r[i] holds window bits [16*i, 16*i + 32).
+// r[0], r[2], r[4] are funnel shifts of the stream words by the lane's offset;
+// r[1], r[3] are byte permutes of their neighbours.
 struct Aligned {
-  uint32_t a0, a1, a2;
+  uint32_t r[5];
 };
 
 template <int BITS>
 __device__ __forceinline__ Aligned align_window(uint32_t w0, uint32_t w1, uint32_t w2, int off) {
   Aligned a;
-  a.a0 = __funnelshift_r(w0, w1, off);
-  a.a1 = __funnelshift_r(w1, w2, off);
-  a.a2 = (BITS >= 7) ? (w2 >> off) : 0u;
+  a.r[0] = __funnelshift_r(w0, w1, off);
+  a.r[2] = (BITS >= 3) ? __funnelshift_r(w1, w2, off) : 0u;
+  a.r[4] = (BITS >= 7) ? (w2 >> off) : 0u;
+  a.r[1] = (BITS >= 3) ? __byte_perm(a.r[0], a.r[2], 0x5432) : 0u;
+  a.r[3] = (BITS >= 6) ? __byte_perm(a.r[2], a.r[4], 0x5432) : 0u;
   return a;
 }
 
-// State of the lane's J-th value (J = 0..7): bits [J*BITS, J*BITS+16) of the aligned window.
-template <int BITS, int J>
-__device__ __forceinline__ uint32_t window_state(const Aligned& a) {
+// State of the lane's J-th value (J = 0..7): bits [J*BITS, J*BITS+16) of the
+// window, read from the view r[i] that holds it at offset q = J*BITS - 16*i in
+// 0..16.  q = 0 is one mask and q = 16 one shift.  Otherwise the bits above the
+// state are dropped either by a shift (ALU pipe) or by a multiply with 2^(16-q)
+// (integer multiply pipe), and those below by a right shift of 16.  The
+// codebooks that hash with a multiply only (3inst, mcg) take the multiply form
+// so both half-rate pipes carry about the same load; mul1, whose byte sum and
+// fp16 fma already load the multiply pipe, takes the shift form.
+template <int BITS, int J, int CB>
+__device__ __forceinline__ uint32_t window_state(const Aligned& a, const MulConsts& mc) {
   constexpr int p = J * BITS;
-  if constexpr (p + 16 <= 32) {
-    return (a.a0 >> p) & 0xFFFFu;
-  } else if constexpr (p < 32) {
-    return __funnelshift_r(a.a0, a.a1, p) & 0xFFFFu;
-  } else if constexpr (p + 16 <= 64) {
-    return (a.a1 >> (p - 32)) & 0xFFFFu;
-  } else if constexpr (p < 64) {
-    return __funnelshift_r(a.a1, a.a2, p - 32) & 0xFFFFu;
+  constexpr int i = (p % 16 == 0 && p >= 16) ? (p / 16 - 1) : (p / 16);  // prefer q = 16 over q = 0
+  constexpr int q = p - 16 * i;
+  static_assert(q >= 0 && q <= 16 && i <= 4, "state outside the window views");
+  const uint32_t v = a.r[i];
+  if constexpr (q == 16) {
+    return v >> 16;
+  } else if constexpr (q == 0) {
+    return v & 0xFFFFu;
+  } else if constexpr (CB == CB_MUL1) {
+    return (v >> q) & 0xFFFFu;
   } else {
-    return (a.a2 >> (p - 64)) & 0xFFFFu;
+    return (v * mc.pow2[16 - q]) >> 16;
   }
 }
 
@@ -148,11 +173,11 @@ __device__ __forceinline__ uint32_t window_state(const Aligned& a) {
 // (TensorFold PR #740, "Arithmetic" step 2: a tile's value order is that of the
 // B fragments of two mma.m16n8k16).
 template <int BITS, int CB>
-__device__ __forceinline__ void decode_lane(const Aligned& a, uint32_t b[4]) {
-  b[0] = decode_pair<CB>(window_state<BITS, 0>(a), window_state<BITS, 1>(a));
-  b[1] = decode_pair<CB>(window_state<BITS, 2>(a), window_state<BITS, 3>(a));
-  b[2] = decode_pair<CB>(window_state<BITS, 4>(a), window_state<BITS, 5>(a));
-  b[3] = decode_pair<CB>(window_state<BITS, 6>(a), window_state<BITS, 7>(a));
+__device__ __forceinline__ void decode_lane(const Aligned& a, const MulConsts& mc, uint32_t b[4]) {
+  b[0] = decode_pair<CB>(window_state<BITS, 0, CB>(a, mc), window_state<BITS, 1, CB>(a, mc));
+  b[1] = decode_pair<CB>(window_state<BITS, 2, CB>(a, mc), window_state<BITS, 3, CB>(a, mc));
+  b[2] = decode_pair<CB>(window_state<BITS, 4, CB>(a, mc), window_state<BITS, 5, CB>(a, mc));
+  b[3] = decode_pair<CB>(window_state<BITS, 6, CB>(a, mc), window_state<BITS, 7, CB>(a, mc));
 }
 
 // Load the lane's window words of one tile (tile_words = first 32-bit word of the tile).

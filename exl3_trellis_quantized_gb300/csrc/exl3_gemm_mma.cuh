@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemm_mma_kernel(const GemmArgs
   const int64_t nt = (c0 >> 4) + warp;
   const uint32_t* tr32 = reinterpret_cast<const uint32_t*>(a.trellis);
   const LaneWindow<BITS> lw(lane);
+  const MulConsts mc(a.one);
   const int64_t kt_begin = kb0 * 8;
   const int64_t kt_last = kb1 * 8 - 1;
 
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemm_mma_kernel(const GemmArgs
       const Aligned al = align_window<BITS>(wr[j & 3][0], wr[j & 3][1], wr[j & 3][2], lw.off);
       load_words(kt + 4, wr[j & 3]);
       uint32_t b[4];
-      decode_lane<BITS, CB>(al, b);
+      decode_lane<BITS, CB>(al, mc, b);
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         uint32_t af[4];

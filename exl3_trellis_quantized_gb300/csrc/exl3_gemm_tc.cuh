@@ -30,7 +30,7 @@
 
 namespace exl3 {
 
-constexpr int kTcDecodeWarps = 8;   // decoder / epilogue warps
+constexpr int kTcDecodeWarps = 16;  // decoder / epilogue warps
 constexpr int kTcThreads = 32 * (2 + kTcDecodeWarps);
 constexpr int kTcSmemBudget = 227 * 1024;
 
@@ -41,6 +41,7 @@ struct TcCfg {
   static constexpr int kTrRowBytes = (BN / 16) * 32 * BITS;  // one k16 row of BN/16 tiles
   static constexpr int kTrBytes = 4 * kTrRowBytes;          // four k16 rows per stage
   static constexpr int kStageBytes = RG * kXBytes + kWBytes + kTrBytes;
+  static constexpr int kZStride = 128 + 4;  // fp32 row stride of the epilogue staging tile
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kStages0 = (kTcSmemBudget - 1024 - kCtrlBytes) / kStageBytes;
   static constexpr int kStages = kStages0 > 6 ? 6 : kStages0;
@@ -48,6 +49,7 @@ struct TcCfg {
   static constexpr int kTmemCols = RG * BN <= 128 ? 128 : (RG * BN <= 256 ? 256 : 512);
   static_assert(RG * BN <= 512, "accumulators exceed tensor memory");
   static_assert(kStages >= 2, "not enough shared memory for two stages");
+  static_assert(128 * kZStride * 4 <= kStages * kStageBytes, "epilogue tile must fit in the stage buffers");
 };
 
 
@@ -155,6 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- decoders ----------------
     const int dw = warp - 2;
     const LaneWindow<BITS> lw(lane);
+    const MulConsts mc(a.one);
     const int row_in = (lane & 7) + ((lane >> 4) << 3);  // stmatrix row of this lane within a 16-row tile
     const int chunk_hi = (lane >> 3) & 1;                // second 8-wide k half
     constexpr int kTilesN = BN / 16;
@@ -164,13 +167,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (!mbar_wait(&full[s], ph)) break;
       const uint32_t* trw = reinterpret_cast<const uint32_t*>(tr_stage(s));
       const uint32_t wbase = smem_u32(w_stage(s));
+      // all window words of this warp's tiles first, so their latency overlaps
+      constexpr int kTpw = 4 * kTilesN / kTcDecodeWarps;  // tiles per warp per stage
+      uint32_t wv[kTpw][3];
 #pragma unroll
-      for (int t = dw; t < 4 * kTilesN; t += kTcDecodeWarps) {
+      for (int i = 0; i < kTpw; ++i) {
+        const int t = dw + i * kTcDecodeWarps;
+        const uint32_t* tile = trw + t * (8 * BITS);
+        wv[i][0] = tile[lw.idx[0]];
+        wv[i][1] = tile[lw.idx[1]];
+        wv[i][2] = (LaneWindow<BITS>::kNeed == 3) ? tile[lw.idx[2]] : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < kTpw; ++i) {
+        const int t = dw + i * kTcDecodeWarps;
         const int kt_l = t / kTilesN;
         const int nt_l = t - kt_l * kTilesN;
-        const Aligned al = load_lane_window<BITS>(trw + (kt_l * kTilesN + nt_l) * (8 * BITS), lw);
+        const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
         uint32_t b[4];
-        decode_lane<BITS, CB>(al, b);
+        decode_lane<BITS, CB>(al, mc, b);
         const int row = nt_l * 16 + row_in;
         const int chunk = 2 * kt_l + chunk_hi;
         stmatrix_x4(wbase + row * 128 + ((chunk ^ (row & 7)) << 4), b[0], b[1], b[2], b[3]);
@@ -181,59 +196,55 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 
     // ---------------- epilogue ----------------
-    const bool ok = mbar_wait(accfull, 0) && *failed == 0u;
+    // Per 128x128 accumulator block: every decoder warp copies a 32-row x
+    // 32-column piece of tensor memory into a shared fp32 tile (the pipeline
+    // stages are free once the accumulators are final), then each warp takes
+    // whole rows, lane l holding columns 4l..4l+3, and runs the same 128-point
+    // butterfly, scale and rounding as the other epilogues.
+    bool ok = mbar_wait(accfull, 0) && *failed == 0u;
     tc_fence_after();
-    const int quarter = warp & 3;
-    const int grp = dw >> 2;
-    constexpr int kJobs = RG * (BN / 128);
+    float* zs = reinterpret_cast<float*>(stages);
+    const int quarter = warp & 3;          // tensor-memory lanes this warp may read
+    const int cchunk = dw >> 2;            // which 32-column piece it copies
+    constexpr int kZ = C::kZStride;
     const bool bf16 = a.y_bf16 != 0;
     uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
-    for (int job = grp; job < kJobs; job += 2) {
-      __syncwarp();
-      const int r = job / (BN / 128);
-      const int hb = job - r * (BN / 128);
-      const int64_t row = row0 + r * 128 + quarter * 32 + lane;
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + hb * 128);
-      float v[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+    constexpr int kBlocks = RG * (BN / 128);
+    for (int blk = 0; blk < kBlocks; ++blk) {
+      const int r = blk / (BN / 128);
+      const int hb = blk - r * (BN / 128);
+      {
         uint32_t q[32];
-        tmem_ld_32x32b_x32(taddr + c * 32, q);
+        tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + hb * 128 + cchunk * 32), q);
         tmem_ld_wait();
+        float* dst = zs + (quarter * 32 + lane) * kZ + cchunk * 32;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[c * 32 + i] = __uint_as_float(q[i]);
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(__uint_as_float(q[i]), __uint_as_float(q[i + 1]),
+                                                            __uint_as_float(q[i + 2]), __uint_as_float(q[i + 3]));
       }
-      if (!ok || row >= a.m) continue;  // after the warp-collective loads
-      // 128-point butterfly, strides 1, 2, ..., 64; (a, b) -> (a + b, a - b)
+      named_barrier(1, 32 * kTcDecodeWarps);
+      const int64_t col = c0 + hb * 128 + 4 * lane;
+      const uint2 sv = *reinterpret_cast<const uint2*>(a.svh + col);
+      const float svf[4] = {__half2float(__ushort_as_half((uint16_t)(sv.x & 0xFFFF))),
+                            __half2float(__ushort_as_half((uint16_t)(sv.x >> 16))),
+                            __half2float(__ushort_as_half((uint16_t)(sv.y & 0xFFFF))),
+                            __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)))};
+      for (int rr = dw; rr < 128; rr += kTcDecodeWarps) {
+        const int64_t row = row0 + r * 128 + rr;
+        if (!ok || row >= a.m) break;  // rows ascend with rr
+        const float4 z4 = *reinterpret_cast<const float4*>(zs + rr * kZ + 4 * lane);
+        float v[4] = {z4.x, z4.y, z4.z, z4.w};
+        fwht128_warp(v, lane);
+        uint16_t o[4];
 #pragma unroll
-      for (int h = 1; h < 128; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          if ((i & h) == 0) {
-            const float x0 = v[i], x1 = v[i + h];
-            v[i] = x0 + x1;
-            v[i + h] = x0 - x1;
-          }
-        }
+        for (int i = 0; i < 4; ++i) o[i] = f32_to_out((v[i] * 0.125f) * svf[i], bf16);
+        uint2 w;
+        w.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
+        w.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
+        *reinterpret_cast<uint2*>(y + row * a.n + col) = w;
       }
-      const int64_t col = c0 + hb * 128;
-      const uint4* sv = reinterpret_cast<const uint4*>(a.svh + col);
-      uint4* dst = reinterpret_cast<uint4*>(y + row * a.n + col);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint4 s8 = sv[c];
-        const uint32_t sw[4] = {s8.x, s8.y, s8.z, s8.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float s_lo = __half2float(__ushort_as_half((uint16_t)(sw[i] & 0xFFFF)));
-          const float s_hi = __half2float(__ushort_as_half((uint16_t)(sw[i] >> 16)));
-          const uint16_t lo = f32_to_out((v[c * 8 + 2 * i] * 0.125f) * s_lo, bf16);
-          const uint16_t hi = f32_to_out((v[c * 8 + 2 * i + 1] * 0.125f) * s_hi, bf16);
-          o[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-        }
-        dst[c] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
+      named_barrier(1, 32 * kTcDecodeWarps);  // the tile is reused by the next block
     }
   }
 

@@ -89,7 +89,8 @@ cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream) {
 
 // One warp per tile; lane l writes its 8 values at their (k, n) positions.
 template <int BITS, int CB>
-__global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t k, int64_t n, uint16_t* wq) {
+__global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t k, int64_t n, uint16_t* wq,
+                                   uint32_t one) {
   const int lane = threadIdx.x & 31;
   const int64_t NT = n >> 4;
   const int64_t tiles = (k >> 4) * NT;
@@ -98,9 +99,10 @@ __global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t 
   const int64_t kt = tile / NT, nt = tile - kt * NT;
   const LaneWindow<BITS> lw(lane);
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(trellis) + tile * (8 * BITS);
+  const MulConsts mc(one);
   const Aligned al = load_lane_window<BITS>(tw, lw);
   uint32_t b[4];
-  decode_lane<BITS, CB>(al, b);
+  decode_lane<BITS, CB>(al, mc, b);
   const int g = lane >> 2, q = lane & 3;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
@@ -116,9 +118,9 @@ static cudaError_t launch_unpack_bits(const int16_t* t, int cb, int64_t k, int64
                                       cudaStream_t stream) {
   const int64_t tiles = (k >> 4) * (n >> 4);
   const unsigned blocks = (unsigned)((tiles + 7) / 8);
-  if (cb == CB_3INST) test_unpack_kernel<BITS, CB_3INST><<<blocks, 256, 0, stream>>>(t, k, n, wq);
-  else if (cb == CB_MCG) test_unpack_kernel<BITS, CB_MCG><<<blocks, 256, 0, stream>>>(t, k, n, wq);
-  else test_unpack_kernel<BITS, CB_MUL1><<<blocks, 256, 0, stream>>>(t, k, n, wq);
+  if (cb == CB_3INST) test_unpack_kernel<BITS, CB_3INST><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
+  else if (cb == CB_MCG) test_unpack_kernel<BITS, CB_MCG><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
+  else test_unpack_kernel<BITS, CB_MUL1><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,7 @@ struct GemmArgs {
   int32_t num_shards;
   int32_t parts;  // P (1 = no split)
   int32_t y_bf16;
+  uint32_t one;  // always 1: seeds the decoder's multiplier constants at run time
 };
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,

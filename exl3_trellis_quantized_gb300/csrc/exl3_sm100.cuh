@@ -56,12 +56,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// try_wait with a suspend-time hint: a waiting thread sleeps (up to the hint, in
+// ns) instead of re-polling, so waiting warps do not take issue slots.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
@@ -112,10 +115,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // stmatrix: store four 8x8 b16 matrices; lane i gives the row address of
 // row (i % 8) of matrix (i / 8); register j holds the lane's pair of matrix j.
 // ---------------------------------------------------------------------------
+// No "memory" clobber: the stores go to the decoded-operand buffer, which no
+// plain load reads, and keeping the clobber would stop the compiler from
+// hoisting the next tile's window loads above this store.  The volatile asm
+// statements that follow (proxy fence, mbarrier arrive) stay ordered after it.
 __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
   asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
-               "r"(r2), "r"(r3)
-               : "memory");
+               "r"(r2), "r"(r3));
 }
 
 // ---------------------------------------------------------------------------
@@ -165,6 +171,11 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Named barrier over a subset of the CTA's warps (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 // Instruction descriptor, kind::f16: D = fp32, A = B = fp16, both K-major,
 // N >> 3 at bits 17..22, M >> 4 at bits 24..28.
