@@ -16,8 +16,8 @@ namespace exl3 {
 // mcg multiply with an increment of 1 and mul1 as the same multiplier followed
 // by a byte sum and one fp16 fused multiply-add (TensorFold PR #740,
 // "Arithmetic" step 2).  The half mask/xor put each 16-bit half in +-[2^-3, 2),
-// so every state decodes finite (cuda-exl3 README, "Loading into a dim vLLM
-// has padded": all 65,536 codes decode finite).
+// so every state decodes to a finite value, as the cuda-exl3 README requires of
+// all 65,536 states ("Loading into a dim vLLM has padded").
 // ---------------------------------------------------------------------------
 constexpr uint32_t kMcgMult = 0xCBAC1FEDu;
 constexpr uint32_t k3instMult = 0xCBAC1FEDu;
@@ -170,8 +170,8 @@ __device__ __forceinline__ uint32_t window_state(const Aligned& a, const MulCons
 
 // The lane's 8 values as 4 half2 registers, in mma.m16n8k16 B-fragment order:
 // b[0] = {k=2q, 2q+1; n=g}, b[1] = {k=2q+8, 2q+9; n=g}, b[2], b[3] = same for n=g+8
-// (TensorFold PR #740, "Arithmetic" step 2: a tile's value order is that of the
-// B fragments of two mma.m16n8k16).
+// (TensorFold PR #740, "Arithmetic" step 2: tiles decode directly into the B
+// fragments of two mma.m16n8k16, which fixes the order of a tile's values).
 template <int BITS, int CB>
 __device__ __forceinline__ void decode_lane(const Aligned& a, const MulConsts& mc, uint32_t b[4]) {
   b[0] = decode_pair<CB>(window_state<BITS, 0, CB>(a, mc), window_state<BITS, 1, CB>(a, mc));

@@ -7,9 +7,8 @@
 // (kt, nt), decodes its 8 values straight into the two B fragments of the n8
 // halves, and multiplies them against every 16-row A fragment of the CTA's rows,
 // so each tile is decoded exactly once per CTA (cuda-exl3 README, "What
-// profiling found": a 16-wide warp tile decodes each tile once; "Why custom
-// kernels": a block owns BM rows x BN columns and the whole k extent, reading its
-// trellis slice once).  The activations xh stream through shared memory with
+// profiling found": a warp tile one tile wide avoids decoding a tile twice;
+// "Why custom kernels": a block covering all of k streams its trellis once).  The activations xh stream through shared memory with
 // cp.async in 128-wide chunks, double-buffered.
 //
 // Epilogue (parts == 1): fp32 z -> shared -> per-row 128-point butterfly ->

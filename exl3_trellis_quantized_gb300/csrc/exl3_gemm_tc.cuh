@@ -1,9 +1,9 @@
 // exl3_gemm_tc.cuh -- EXL3 GEMM on the 5th-generation tensor cores (tcgen05).
 //
 // One CTA owns BN output columns (BN/128 output Hadamard blocks) and RG*128
-// rows over the whole k extent (cuda-exl3 README, "Why custom kernels": a block
-// owns BM rows x BN columns and the whole k, reads its trellis slice once and
-// folds the output Hadamard and svh into the epilogue).  Warp roles:
+// rows over the whole k extent.  Owning all of k lets a block stream its share
+// of the trellis a single time and apply the output Hadamard and svh in its
+// epilogue (cuda-exl3 README, "Why custom kernels").  Warp roles:
 //
 //   warp 0      TMA producer: per 64-wide k stage, four 1-D bulk copies of the
 //               stage's trellis tile rows and RG tiled copies of the rotated

@@ -18,9 +18,9 @@ cudaError_t launch_gemm_mma(const GemmArgs& args, int bits, int cb, cudaStream_t
   }
 }
 
-// Split-k epilogue (cuda-exl3 README, "One op per layer": the epilogue Hadamard
-// consumes the fp32 partials and re-zeroes the buffer; TensorFold PR #740: parts
-// are added in part order).  One warp per (row, 128-column block); lane l owns
+// Split-k epilogue (cuda-exl3 README, "One op per layer": a second kernel turns
+// the fp32 partials into outputs and leaves the buffer zeroed for the next call;
+// TensorFold PR #740, "Arithmetic": parts are summed in a fixed part order).  One warp per (row, 128-column block); lane l owns
 // columns 4l..4l+3 of the block: z = ((p0 + p1) + p2) + ..., then the same
 // butterfly, scale and rounding as the fused epilogue, then zeros written back.
 __global__ void __launch_bounds__(256) splitk_epilogue_kernel(const GemmArgs a) {

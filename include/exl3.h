@@ -99,8 +99,8 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
 
 /*
  * Split-k variant.  cuda-exl3 README, "One op per layer" (split-k for narrow
- * layers: partials into an fp32 accumulator, an epilogue kernel does the
- * Hadamard and re-zeroes the buffer); TensorFold PR #740, "Arithmetic" (k
+ * layers: partials go to an fp32 accumulator that a second kernel turns into
+ * outputs while zeroing it again); TensorFold PR #740, "Arithmetic" (k
  * blocks split into a number of parts fixed by the shape, parts added in part
  * order).  Part p covers a contiguous range of whole 128-row blocks of k; its
  * fp32 partial goes to acc[p][r][c]; the epilogue sums p = 0..P-1 in order,

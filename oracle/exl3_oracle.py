@@ -56,12 +56,12 @@ def f64_to_half_bits(x) -> np.ndarray:
 # ---------------------------------------------------------------------------
 
 # mcg multiplier, printed with the GLM-5.3-Flash checkpoint description
-# (cuda-exl3 README, "GLM-5.3-Flash": "multiplier 0xCBAC1FED").
+# (cuda-exl3 README, section "GLM-5.3-Flash").
 MCG_MULT = 0xCBAC1FED
 
 # Reading (the pages give no 3inst or mul1 constants): 3inst is the mcg map
 # with an increment, i.e. one multiply-add, the mask/xor and the half add
-# ("three instructions"); mul1 uses the same multiplier.
+# (which is what the codebook's name suggests); mul1 uses the same multiplier.
 INST3_MULT = 0xCBAC1FED
 INST3_ADD = 1
 MUL1_MULT = 0xCBAC1FED
@@ -69,13 +69,13 @@ MUL1_MULT = 0xCBAC1FED
 # Reading: the mask keeps sign, the two low exponent bits and the mantissa of
 # each 16-bit half; the xor sets the exponent field to 0b011xx, so each half
 # lies in +-[2^-3, 2).  This makes every state decode to a finite value, the
-# totality the cuda-exl3 README states ("all 65,536 codes decode finite in
-# every codebook").
+# totality the cuda-exl3 README states for all 65,536 states of every codebook
+# ("Loading into a dim vLLM has padded").
 HALF_MASK = 0x8FFF8FFF
 HALF_XOR = 0x30003000
 
-# Reading for mul1 (TensorFold PR, "Arithmetic": "one fused fp16
-# multiply-add of an exact sum, the single rounding the format specifies"):
+# Reading for mul1 (TensorFold PR, "Arithmetic": the value comes from one fp16
+# fused multiply-add applied to an exactly computed sum, so it is rounded once):
 # the exact sum is the sum of the four bytes of the hashed state (0..1020);
 # the affine map standardises a sum of four uniform bytes (mean 510,
 # sd sqrt(4*(256^2-1)/12) ~= 147.8).  Both coefficients are fp16 numbers.
@@ -139,9 +139,9 @@ def codebook(cb: int, states) -> np.ndarray:
 def tile_position(v: int):
     """(k, n) inside a 16x16 tile of the tile's v-th decoded value.
 
-    The tile's value order is that of the B operands of two
-    mma.m16n8k16 instructions (TensorFold PR, "Arithmetic" step 2), each
-    lane holding 8 consecutive values (cuda-exl3 README, "Where the time
+    Tiles decode directly into the B operands of two mma.m16n8k16
+    instructions, which fixes the value order (TensorFold PR, "Arithmetic"
+    step 2), each lane holding 8 consecutive values (cuda-exl3 README, "Where the time
     goes": lane*8 alignment).  Lane l = v // 8 holds, for each n8 half h,
     the fragment registers b0 = (k = 2q, 2q+1) and b1 = (k = 2q+8, 2q+9) of
     column n = l // 4 + 8h, with q = l % 4.  Reading: the 8 values of a lane
