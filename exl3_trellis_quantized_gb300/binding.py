@@ -45,6 +45,8 @@ def lib() -> ctypes.CDLL:
     L.exl3_input_transform.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
     L.exl3_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, ctypes.c_int, i64, vp]
     L.exl3_gemm_splitk.argtypes = L.exl3_gemm.argtypes[:-1] + [vp, sz, vp]
+    L.exl3_gemm_splitk_noalloc.argtypes = L.exl3_gemm.argtypes
+    L.exl3_gemm_splitk_noalloc.restype = ctypes.c_int
     L.exl3_splitk_parts.argtypes = [i64, i64]
     L.exl3_splitk_parts.restype = i32
     L.exl3_splitk_workspace_bytes.argtypes = [i64, i64, i64]
@@ -163,6 +165,29 @@ def gemm_splitk(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: tor
                                 _BF16 if out.dtype == torch.bfloat16 else _F16, n, _ptr(acc),
                                 acc.numel() * 4, _stream(xh))
     _check(st, "exl3_gemm_splitk")
+    return out
+
+
+# Size of the library's built-in split-k scratch (EXL3_NOALLOC_SCRATCH_BYTES in include/exl3.h).
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def gemm_splitk_noalloc(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor,
+                        shard_cols: Sequence[int], out_dtype=torch.bfloat16,
+                        out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Split-k GEMM whose partials live in the library's built-in scratch array.
+
+    For callers that cannot allocate a workspace.  Requests whose workspace
+    would exceed NOALLOC_SCRATCH_BYTES are refused; calls must not overlap on
+    the GPU (they share the one array).
+    """
+    m, k, n, cols, ns, cbid, out = _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+    st = lib().exl3_gemm_splitk_noalloc(_ptr(xh), m, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(out),
+                                        _BF16 if out.dtype == torch.bfloat16 else _F16, n, _stream(xh))
+    if st == 3:
+        raise Exl3Error(st, f"exl3_gemm_splitk_noalloc (needs {splitk_workspace_bytes(m, k, n)} bytes of scratch, "
+                            f"the built-in array holds {NOALLOC_SCRATCH_BYTES})")
+    _check(st, "exl3_gemm_splitk_noalloc")
     return out
 
 

@@ -125,6 +125,35 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
                                void* stream);
 
 /*
+ * exl3_gemm_splitk_noalloc -- the split-k GEMM for callers that cannot allocate.
+ *
+ * The pages have no counterpart to this call; it exists for callers that have
+ * no way to obtain a device workspace (a plugin inside a host program that owns
+ * the allocator, or code that must not call cudaMalloc because it would
+ * synchronise the device or break a fixed memory budget).  It computes exactly
+ * what exl3_gemm_splitk computes, with the same arguments minus the workspace:
+ * the fp32 partials go to a scratch array built into the library, of
+ * EXL3_NOALLOC_SCRATCH_BYTES per GPU, held on every GPU that loads the library
+ * until the process exits.  It calls no allocator.
+ *
+ *  - Size limit: exl3_splitk_workspace_bytes(m, k, n) must not exceed
+ *    EXL3_NOALLOC_SCRATCH_BYTES; a larger request returns EXL3_EWORKSPACE and
+ *    launches nothing (use exl3_gemm_splitk with your own workspace instead).
+ *  - The first call on a device looks up the scratch array's device address
+ *    (with that device current) and caches it; make that first call before any
+ *    stream capture on that device.
+ *  - Every call shares the one array.  Calls whose work may overlap on the GPU
+ *    (different streams, or different threads without ordering) race on it and
+ *    give wrong results; order them on one stream.  Each call overwrites every
+ *    partial it reads, so what an earlier call left behind does no harm.
+ */
+#define EXL3_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+exl3_status_t exl3_gemm_splitk_noalloc(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis,
+                                       int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
+                                       const int32_t* shard_cols, int32_t num_shards, void* y,
+                                       exl3_dtype_t y_dtype, int64_t n, void* stream);
+
+/*
  * Test-only entry points (they run the same device decode as exl3_gemm).
  *
  * exl3_test_codebook: out[s] = fp16 bits of codebook cb at state s, s = 0..65535
