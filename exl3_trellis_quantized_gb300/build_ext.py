@@ -32,7 +32,6 @@ def units():
     for name in ("exl3_api.cu", "exl3_transform.cu", "exl3_kernels_misc.cu", "exl3_tc_host.cu", "exl3_noalloc.cu"):
         out.append((name, name.replace(".cu", ".o"), []))
     for b in range(1, 9):
-        out.append(("exl3_gemm_mma_inst.cu", f"exl3_gemm_mma_b{b}.o", [f"-DEXL3_INST_BITS={b}"]))
         out.append(("exl3_gemm_tc_inst.cu", f"exl3_gemm_tc_b{b}.o", [f"-DEXL3_INST_BITS={b}"]))
     return out
 

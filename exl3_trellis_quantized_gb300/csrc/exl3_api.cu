@@ -63,7 +63,7 @@ exl3_status_t check_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t
   for (int i = 0; i <= num_shards; ++i) a->shard_cols[i] = shard_cols[i];
   a->parts = 1;
   a->y_bf16 = (y_dtype == EXL3_BF16) ? 1 : 0;
-  a->one = 1u;
+  exl3::fill_decode_consts(&a->dc);
   return EXL3_OK;
 }
 
@@ -141,7 +141,7 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
     // one part: the fused epilogue already does everything; acc stays zero
     return cuda_status(exl3::launch_gemm_tc(a, bits, cb, s), "exl3_gemm_splitk");
   }
-  st = cuda_status(exl3::launch_gemm_mma(a, bits, cb, s), "exl3_gemm_splitk parts");
+  st = cuda_status(exl3::launch_gemm_tc(a, bits, cb, s), "exl3_gemm_splitk parts");
   if (st != EXL3_OK) return st;
   return cuda_status(exl3::launch_splitk_epilogue(a, s), "exl3_gemm_splitk epilogue");
 }

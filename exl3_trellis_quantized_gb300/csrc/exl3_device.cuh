@@ -7,6 +7,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "exl3_launch.h"
+
 namespace exl3 {
 
 // ---------------------------------------------------------------------------
@@ -49,8 +51,12 @@ __device__ __forceinline__ uint32_t hfma2_u32(uint32_t a, uint32_t b, uint32_t c
   asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+// (u & kHalfMask) ^ kHalfXor as one three-input logic op (truth table 0x6A:
+// a & b ^ c), written out so that it is never split into two operations.
 __device__ __forceinline__ uint32_t lop3_mask_xor(uint32_t u) {
-  return (u & kHalfMask) ^ kHalfXor;  // one LOP3
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(u), "n"(kHalfMask), "n"(kHalfXor));
+  return d;
 }
 
 // Two states -> one half2 register {value(s0) in bits 0..15, value(s1) in bits 16..31}.
@@ -112,18 +118,6 @@ struct LaneWindow {
   }
 };
 
-// Multipliers the decoder uses for shifts it runs on the integer multiply-add
-// pipe.  They are derived at run time from a kernel argument equal to 1 so the
-// compiler keeps them as multiplies (the ALU pipe that executes shifts, masks
-// and permutes is the decoder's bottleneck; IMAD runs on a separate pipe).
-struct MulConsts {
-  uint32_t pow2[17];  // pow2[i] = 1 << i
-  __device__ __forceinline__ explicit MulConsts(uint32_t one) {
-#pragma unroll
-    for (int i = 0; i <= 16; ++i) pow2[i] = one << i;
-  }
-};
-
 // Aligned views of a lane's window: r[i] holds window bits [16*i, 16*i + 32).
 // r[0], r[2], r[4] are funnel shifts of the stream words by the lane's offset;
 // r[1], r[3] are byte permutes of their neighbours.
@@ -151,7 +145,7 @@ __device__ __forceinline__ Aligned align_window(uint32_t w0, uint32_t w1, uint32
 // so both half-rate pipes carry about the same load; mul1, whose byte sum and
 // fp16 fma already load the multiply pipe, takes the shift form.
 template <int BITS, int J, int CB>
-__device__ __forceinline__ uint32_t window_state(const Aligned& a, const MulConsts& mc) {
+__device__ __forceinline__ uint32_t window_state(const Aligned& a, const DecodeConsts& mc) {
   constexpr int p = J * BITS;
   constexpr int i = (p % 16 == 0 && p >= 16) ? (p / 16 - 1) : (p / 16);  // prefer q = 16 over q = 0
   constexpr int q = p - 16 * i;
@@ -173,7 +167,7 @@ __device__ __forceinline__ uint32_t window_state(const Aligned& a, const MulCons
 // (TensorFold PR #740, "Arithmetic" step 2: tiles decode directly into the B
 // fragments of two mma.m16n8k16, which fixes the order of a tile's values).
 template <int BITS, int CB>
-__device__ __forceinline__ void decode_lane(const Aligned& a, const MulConsts& mc, uint32_t b[4]) {
+__device__ __forceinline__ void decode_lane(const Aligned& a, const DecodeConsts& mc, uint32_t b[4]) {
   b[0] = decode_pair<CB>(window_state<BITS, 0, CB>(a, mc), window_state<BITS, 1, CB>(a, mc));
   b[1] = decode_pair<CB>(window_state<BITS, 2, CB>(a, mc), window_state<BITS, 3, CB>(a, mc));
   b[2] = decode_pair<CB>(window_state<BITS, 4, CB>(a, mc), window_state<BITS, 5, CB>(a, mc));

@@ -7,7 +7,7 @@
 #endif
 
 namespace exl3 {
-template cudaError_t launch_gemm_tc_bits<EXL3_INST_BITS>(const CUtensorMap&, const TcParams&, int, int, int,
+template cudaError_t launch_gemm_tc_bits<EXL3_INST_BITS>(const TcMaps&, const TcParams&, int, TcShape,
                                                          cudaStream_t);
 
 // This translation unit's wait-timeout flag (see exl3_sm100.cuh).

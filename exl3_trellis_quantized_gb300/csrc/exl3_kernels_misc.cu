@@ -1,22 +1,8 @@
-// exl3_kernels_misc.cu -- width dispatch of the GEMM, the split-k epilogue and
-// the test-only decode kernels.
+// exl3_kernels_misc.cu -- the split-k epilogue and the test-only decode kernels.
 #include "exl3_device.cuh"
 #include "exl3_launch.h"
 
 namespace exl3 {
-
-cudaError_t launch_gemm_mma(const GemmArgs& args, int bits, int cb, cudaStream_t stream) {
-  switch (bits) {
-    case 1: return launch_gemm_mma_bits<1>(args, cb, stream);
-    case 2: return launch_gemm_mma_bits<2>(args, cb, stream);
-    case 3: return launch_gemm_mma_bits<3>(args, cb, stream);
-    case 4: return launch_gemm_mma_bits<4>(args, cb, stream);
-    case 5: return launch_gemm_mma_bits<5>(args, cb, stream);
-    case 6: return launch_gemm_mma_bits<6>(args, cb, stream);
-    case 7: return launch_gemm_mma_bits<7>(args, cb, stream);
-    default: return launch_gemm_mma_bits<8>(args, cb, stream);
-  }
-}
 
 // Split-k epilogue (cuda-exl3 README, "One op per layer": a second kernel turns
 // the fp32 partials into outputs and leaves the buffer zeroed for the next call;
@@ -90,7 +76,10 @@ cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream) {
 // One warp per tile; lane l writes its 8 values at their (k, n) positions.
 template <int BITS, int CB>
 __global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t k, int64_t n, uint16_t* wq,
-                                   uint32_t one) {
+                                   const DecodeConsts dc) {
+  DecodeConsts mc;
+#pragma unroll
+  for (int i = 0; i <= 16; ++i) mc.pow2[i] = dc.pow2[i];
   const int lane = threadIdx.x & 31;
   const int64_t NT = n >> 4;
   const int64_t tiles = (k >> 4) * NT;
@@ -99,7 +88,6 @@ __global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t 
   const int64_t kt = tile / NT, nt = tile - kt * NT;
   const LaneWindow<BITS> lw(lane);
   const uint32_t* tw = reinterpret_cast<const uint32_t*>(trellis) + tile * (8 * BITS);
-  const MulConsts mc(one);
   const Aligned al = load_lane_window<BITS>(tw, lw);
   uint32_t b[4];
   decode_lane<BITS, CB>(al, mc, b);
@@ -116,11 +104,13 @@ __global__ void test_unpack_kernel(const int16_t* __restrict__ trellis, int64_t 
 template <int BITS>
 static cudaError_t launch_unpack_bits(const int16_t* t, int cb, int64_t k, int64_t n, uint16_t* wq,
                                       cudaStream_t stream) {
+  DecodeConsts dc;
+  fill_decode_consts(&dc);
   const int64_t tiles = (k >> 4) * (n >> 4);
   const unsigned blocks = (unsigned)((tiles + 7) / 8);
-  if (cb == CB_3INST) test_unpack_kernel<BITS, CB_3INST><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
-  else if (cb == CB_MCG) test_unpack_kernel<BITS, CB_MCG><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
-  else test_unpack_kernel<BITS, CB_MUL1><<<blocks, 256, 0, stream>>>(t, k, n, wq, 1u);
+  if (cb == CB_3INST) test_unpack_kernel<BITS, CB_3INST><<<blocks, 256, 0, stream>>>(t, k, n, wq, dc);
+  else if (cb == CB_MCG) test_unpack_kernel<BITS, CB_MCG><<<blocks, 256, 0, stream>>>(t, k, n, wq, dc);
+  else test_unpack_kernel<BITS, CB_MUL1><<<blocks, 256, 0, stream>>>(t, k, n, wq, dc);
   return cudaGetLastError();
 }
 

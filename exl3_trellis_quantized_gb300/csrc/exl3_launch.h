@@ -9,6 +9,17 @@ namespace exl3 {
 
 constexpr int kMaxShards = 8;
 
+// Powers of two the decoder multiplies by when it runs shifts on the integer
+// multiply pipe (the ALU pipe that executes shifts, masks and permutes is the
+// decoder's bottleneck).  They arrive as kernel parameters, so the compiler
+// cannot fold them back into shifts; kernels copy them into registers once.
+struct DecodeConsts {
+  uint32_t pow2[17];  // pow2[i] = 1 << i, filled on the host
+};
+inline void fill_decode_consts(DecodeConsts* dc) {
+  for (int i = 0; i <= 16; ++i) dc->pow2[i] = 1u << i;
+}
+
 // Everything one GEMM launch needs; passed by value as a kernel parameter.
 struct GemmArgs {
   const uint16_t* xh;      // fp16 [S][m][k]
@@ -21,14 +32,11 @@ struct GemmArgs {
   int32_t num_shards;
   int32_t parts;  // P (1 = no split)
   int32_t y_bf16;
-  uint32_t one;  // always 1: seeds the decoder's multiplier constants at run time
+  DecodeConsts dc;
 };
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
                                    int num_shards, uint16_t* xh, cudaStream_t stream);
-
-// mma.sync GEMM mainloop; with args.parts > 1 it writes fp32 partials to args.acc.
-cudaError_t launch_gemm_mma(const GemmArgs& args, int bits, int cb, cudaStream_t stream);
 
 // Sum the P partials in part order, rotate, scale, store y, zero the workspace.
 cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
@@ -37,23 +45,38 @@ cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream);
 cudaError_t launch_test_unpack(const int16_t* trellis, int bits, int cb, int64_t k, int64_t n, uint16_t* wq,
                                cudaStream_t stream);
 
-// tcgen05 GEMM (one translation unit per width); parts > 1 is not handled here.
-constexpr int kTcBK = 64;  // k per pipeline stage (one 128-byte swizzle row of fp16)
+// tcgen05 GEMM (one translation unit per width).
+constexpr int kTcBK = 64;  // k per swizzle atom (one 128-byte row of fp16)
 struct TcParams {
   GemmArgs a;
   int32_t box_rows;  // rows per xh tile copy (<= 128)
 };
+// The tensor maps one tcgen05 launch reads through.
+struct TcMaps {
+  CUtensorMap xh;       // fp16 xh, 4-D {64, m, k/64, S}: KA atoms of box_rows rows per copy
+  CUtensorMap trellis;  // int16 trellis, 3-D {16*bits, n/16, k/16}: a stage's tile rows per copy
+};
+// Tile shapes of the tcgen05 GEMM: columns per CTA (BN), row groups of 128
+// (RG), 64-wide k atoms per pipeline stage (KA) and activation rows held per
+// atom (XR).  Shapes with BN < 128 run as clusters of 128/BN CTAs.
+enum class TcShape : int {
+  kN32Small,   // BN=32,  RG=1, KA=4, XR=32   (m <= 32, narrow layers)
+  kN64Small,   // BN=64,  RG=1, KA=2, XR=32   (m <= 32, wide layers)
+  kN128Small,  // BN=128, RG=1, KA=1, XR=32   (m <= 32, very wide layers, split-k parts)
+  kN128,       // BN=128, RG=1, KA=1, XR=128  (m <= 128)
+  kN128R2,     // BN=128, RG=2, KA=1, XR=128  (large m)
+  kN256R2,     // BN=256, RG=2, KA=1, XR=128  (large m, 256-aligned shard edges)
+};
+// Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
+// (parts > 1) for the split-k epilogue.
 cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream);
 template <int BITS>
-cudaError_t launch_gemm_tc_bits(const CUtensorMap& xmap, const TcParams& p, int cb, int bn, int rg,
+cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, TcShape shape,
                                 cudaStream_t stream);
 // Read and clear the wait-timeout flags of every kernel translation unit (synchronous).
 cudaError_t take_device_errors(uint32_t* flags);
 template <int BITS>
 cudaError_t take_device_error_tc(uint32_t* flags);
 
-// Per-width instantiations of the mma.sync GEMM (one translation unit per width).
-template <int BITS>
-cudaError_t launch_gemm_mma_bits(const GemmArgs& args, int cb, cudaStream_t stream);
 
 }  // namespace exl3

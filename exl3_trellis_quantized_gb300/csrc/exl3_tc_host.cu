@@ -1,5 +1,6 @@
-// exl3_tc_host.cu -- host side of the tcgen05 GEMM: the TMA tensor map of the
-// rotated activations, the tile-shape choice and the width dispatch.
+// exl3_tc_host.cu -- host side of the tcgen05 GEMM: the TMA tensor maps of the
+// rotated activations and of the trellis, the tile-shape choice and the width
+// dispatch.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -26,38 +27,114 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-// xh is fp16 [S][m][k]; tiles are 64 (k) x box_rows (rows) x 1 (shard), 128-byte
-// swizzled, out-of-range rows read as zeros.
-cudaError_t make_xh_map(CUtensorMap* map, const uint16_t* xh, int64_t m, int64_t k, int num_shards, int box_rows) {
+namespace {
+
+// xh is fp16 [S][m][k], viewed as 4-D {64 (k inside an atom), m, k/64 (atoms), S}
+// so that one copy brings KA atoms of box_rows rows each, laid out atom after
+// atom in shared memory, 128-byte swizzled; rows past m read as zeros.
+cudaError_t make_xh_map(CUtensorMap* map, const uint16_t* xh, int64_t m, int64_t k, int num_shards, int box_rows,
+                        int atoms) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
-  cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)m, (cuuint64_t)num_shards};
-  cuuint64_t strides[2] = {(cuuint64_t)k * 2, (cuuint64_t)(m * k * 2)};
-  cuuint32_t box[3] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<uint16_t*>(xh), dims, strides, box, estr,
+  cuuint64_t dims[4] = {(cuuint64_t)kTcBK, (cuuint64_t)m, (cuuint64_t)(k / kTcBK), (cuuint64_t)num_shards};
+  cuuint64_t strides[3] = {(cuuint64_t)k * 2, (cuuint64_t)kTcBK * 2, (cuuint64_t)(m * k * 2)};
+  cuuint32_t box[4] = {(cuuint32_t)kTcBK, (cuuint32_t)box_rows, (cuuint32_t)atoms, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<uint16_t*>(xh), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// trellis is int16 [k/16][n/16][16*bits], viewed as 3-D {16*bits, n/16, k/16}; one
+// copy brings a CTA's bn/16 tiles for rows k16 of a stage, stored row after row.
+cudaError_t make_trellis_map(CUtensorMap* map, const int16_t* trellis, int64_t k, int64_t n, int bits, int bn,
+                             int rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[3] = {(cuuint64_t)(16 * bits), (cuuint64_t)(n / 16), (cuuint64_t)(k / 16)};
+  cuuint64_t strides[2] = {(cuuint64_t)(32 * bits), (cuuint64_t)((n / 16) * 32 * bits)};
+  cuuint32_t box[3] = {(cuuint32_t)(16 * bits), (cuuint32_t)(bn / 16), (cuuint32_t)rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<int16_t*>(trellis), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+struct ShapeDims {
+  int bn, ka, xr;
+};
+
+ShapeDims dims_of(TcShape s) {
+  switch (s) {
+    case TcShape::kN32Small: return {32, 4, 32};
+    case TcShape::kN64Small: return {64, 2, 32};
+    case TcShape::kN128Small: return {128, 2, 32};
+    case TcShape::kN128: return {128, 1, 128};
+    case TcShape::kN128R2: return {128, 1, 128};
+    default: return {256, 1, 128};
+  }
+}
+
+// Tile shape for a call.  Every shape computes each output element with the
+// same sequence of k16 steps, so this choice never changes the result; it only
+// trades parallelism (small batches need many CTAs to reach every SM) against
+// reuse of each decoded tile across rows (large batches).
+// Decode throughput a small-batch CTA reaches on its SM relative to a
+// 128-column CTA, measured on GB300 (q_proj-like layer, m = 16): narrow strips
+// spend more of each SM on the cluster, per-stage synchronisation and the
+// tensor core's 128-row operand reads.
+constexpr double kRel64 = 0.48, kRel32 = 0.43;
+constexpr int64_t kSms = 152;
+
+// Average number of busy SMs over the waves of a grid, times its per-SM rate.
+double small_batch_rate(int64_t ctas, double rel) {
+  const int64_t waves = (ctas + kSms - 1) / kSms;
+  return rel * (double)ctas / (double)waves;
+}
+
+TcShape choose_shape(const GemmArgs& a) {
+  if (a.parts > 1) return a.m <= 32 ? TcShape::kN128Small : (a.m <= 128 ? TcShape::kN128 : TcShape::kN128R2);
+  if (a.m <= 32) {
+    // pick the column width whose grid keeps the most decode throughput busy
+    const double r128 = small_batch_rate(a.n / 128, 1.0);
+    const double r64 = small_batch_rate(a.n / 64, kRel64);
+    // 32-column strips use 4 k atoms per stage: k must hold an even number of 128-blocks
+    const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
+    if (r128 >= r64 && r128 >= r32) return TcShape::kN128Small;
+    return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
+  }
+  if (a.m <= 128) return TcShape::kN128;
+  bool edges256 = (a.n % 256) == 0;
+  for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
+  return edges256 ? TcShape::kN256R2 : TcShape::kN128R2;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  p.box_rows = a.m >= 128 ? 128 : (int)((a.m + 7) / 8 * 8);
-  CUtensorMap map;
-  cudaError_t e = make_xh_map(&map, a.xh, a.m, a.k, a.num_shards, p.box_rows);
+  const TcShape shape = choose_shape(a);
+  const ShapeDims d = dims_of(shape);
+  // rows per activation copy: every allocated row when a stage holds several
+  // atoms (their regions sit back to back), else just the rows in use
+  p.box_rows = d.ka > 1 ? d.xr : (a.m >= d.xr ? d.xr : (int)((a.m + 7) / 8 * 8));
+  TcMaps maps;
+  cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, d.ka);
   if (e != cudaSuccess) return e;
-  const int bn = 128, rg = 1;
+  e = make_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, d.bn, 4 * d.ka);
+  if (e != cudaSuccess) return e;
   switch (bits) {
-    case 1: return launch_gemm_tc_bits<1>(map, p, cb, bn, rg, stream);
-    case 2: return launch_gemm_tc_bits<2>(map, p, cb, bn, rg, stream);
-    case 3: return launch_gemm_tc_bits<3>(map, p, cb, bn, rg, stream);
-    case 4: return launch_gemm_tc_bits<4>(map, p, cb, bn, rg, stream);
-    case 5: return launch_gemm_tc_bits<5>(map, p, cb, bn, rg, stream);
-    case 6: return launch_gemm_tc_bits<6>(map, p, cb, bn, rg, stream);
-    case 7: return launch_gemm_tc_bits<7>(map, p, cb, bn, rg, stream);
-    default: return launch_gemm_tc_bits<8>(map, p, cb, bn, rg, stream);
+    case 1: return launch_gemm_tc_bits<1>(maps, p, cb, shape, stream);
+    case 2: return launch_gemm_tc_bits<2>(maps, p, cb, shape, stream);
+    case 3: return launch_gemm_tc_bits<3>(maps, p, cb, shape, stream);
+    case 4: return launch_gemm_tc_bits<4>(maps, p, cb, shape, stream);
+    case 5: return launch_gemm_tc_bits<5>(maps, p, cb, shape, stream);
+    case 6: return launch_gemm_tc_bits<6>(maps, p, cb, shape, stream);
+    case 7: return launch_gemm_tc_bits<7>(maps, p, cb, shape, stream);
+    default: return launch_gemm_tc_bits<8>(maps, p, cb, shape, stream);
   }
 }
 

@@ -160,6 +160,31 @@ def test_linear_coverage_2048(bits, cb):
         assert torch.equal(ym.view(torch.int16), y[:m].view(torch.int16))
 
 
+SHAPE_CASES = [
+    # k, n, bits, codebook, batch sizes: chosen so the kernel switches tile shapes
+    # (128-column small-batch CTAs, 32/64-column cluster strips, one and two row
+    # groups, 128 and 256 columns) between the batch sizes of one case
+    (1024, 12288, 4, 0, [3, 16, 77, 300]),
+    (1024, 640, 3, 2, [5, 40, 300]),
+    (384, 4096, 5, 1, [2, 20, 150]),  # an odd number of 128-blocks of k
+    (2048, 2048, 6, 1, [1, 33, 129, 257]),
+]
+
+
+@pytest.mark.parametrize("k,n,bits,cb,ms", SHAPE_CASES, ids=[f"{c[0]}x{c[1]}" for c in SHAPE_CASES])
+def test_rows_byte_equal_across_tile_shapes(k, n, bits, cb, ms):
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=3000 + n)
+    x = synthetic.make_x(max(ms), k, seed=3000)
+    y, _ = _run(layer, x, torch.bfloat16, False)
+    for m in ms[:-1]:
+        ym, _ = _run(layer, x, torch.bfloat16, False, m=m)
+        assert torch.equal(ym.view(torch.int16), y[:m].view(torch.int16)), f"row bytes differ at m={m}"
+    blocks = [0, n // 128 - 1]
+    ref = _oracle(x, layer, blocks)
+    got = _np(y).reshape(max(ms), n // 128, 128)[:, blocks].reshape(max(ms), -1)
+    _assert_columns(got, ref)
+
+
 def test_fused_shards_equal_separate_launches():
     k, bits, cb = 512, 5, 2
     layer = synthetic.make_layer(k, [256, 128, 384], bits, cb, seed=77)
