@@ -243,23 +243,25 @@ def run_gpu(args, wl_name):
     sol_step = sum(sol_seconds(m, k, n, bits, peaks)[0] for m in ms)
     value = 100.0 * sol_step * args.steps * world / elapsed
 
-    # dominant GEMM launch: the batch size that takes the longest
+    # dominant GEMM launch: the batch size that takes the longest.  Each batch
+    # size's GEMM runs `reps` times back to back between two events (weights
+    # rotating over the copies, so no launch finds its trellis in L2); the
+    # average launch duration is the span divided by `reps`.
     gemm_s = []
     gev = [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
     for i, m in enumerate(ms):
         E.input_transform(xs[i], suh, xh[i])
-        tot = 0.0
+        torch.cuda.synchronize()
+        gev[0].record(stream)
         for r in range(reps):
-            gev[0].record(stream)
             tr = trs[(r + i) % copies]
             if split:
                 E.gemm_splitk(xh[i], tr, bits, cb, svh, layer.shard_cols, accs[i], out=ys[i])
             else:
                 E.gemm(xh[i], tr, bits, cb, svh, layer.shard_cols, out=ys[i])
-            gev[1].record(stream)
-            torch.cuda.synchronize()
-            tot += gev[0].elapsed_time(gev[1]) / 1e3
-        gemm_s.append(tot / reps)
+        gev[1].record(stream)
+        torch.cuda.synchronize()
+        gemm_s.append(gev[0].elapsed_time(gev[1]) / 1e3 / reps)
     dom = max(range(len(ms)), key=lambda i: gemm_s[i])
     md = ms[dom]
     _, bound = sol_seconds(md, k, n, bits, peaks)

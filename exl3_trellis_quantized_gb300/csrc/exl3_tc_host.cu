@@ -86,15 +86,38 @@ ShapeDims dims_of(TcShape s) {
 // spend more of each SM on the cluster, per-stage synchronisation and the
 // tensor core's 128-row operand reads.
 constexpr double kRel64 = 0.48, kRel32 = 0.43;
-constexpr int64_t kSms = 152;
 
-// Average number of busy SMs over the waves of a grid, times its per-SM rate.
+constexpr double kCost128 = 0.79, kCost256 = 2.26, kCost256Mul1 = 1.72;
+
+// SMs of the current device, read once per device.
+int64_t sm_count() {
+  static std::mutex mu;
+  static int64_t cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int v = 0;
+    cache[dev] = cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0 ? v : 152;
+  }
+  return cache[dev];
+}
+
+// Average number of busy SMs over the waves of a grid (one CTA per SM), times
+// its per-SM rate.
 double small_batch_rate(int64_t ctas, double rel) {
-  const int64_t waves = (ctas + kSms - 1) / kSms;
+  const int64_t sms = sm_count();
+  const int64_t waves = (ctas + sms - 1) / sms;
   return rel * (double)ctas / (double)waves;
 }
 
-TcShape choose_shape(const GemmArgs& a) {
+// Whole waves of a grid times the cost of one of its CTAs.
+double large_batch_time(int64_t ctas, double cost) {
+  const int64_t sms = sm_count();
+  return (double)((ctas + sms - 1) / sms) * cost;
+}
+
+TcShape choose_shape(const GemmArgs& a, int cb) {
   if (a.parts > 1) return a.m <= 32 ? TcShape::kN128Small : (a.m <= 128 ? TcShape::kN128 : TcShape::kN128R2);
   if (a.m <= 32) {
     // pick the column width whose grid keeps the most decode throughput busy
@@ -106,9 +129,19 @@ TcShape choose_shape(const GemmArgs& a) {
     return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
   }
   if (a.m <= 128) return TcShape::kN128;
+  // Larger batches: least estimated time over whole waves.  Per-CTA costs are
+  // relative to a 256-row, 128-column CTA over the same k, measured on GB300
+  // (5120 x 12288 at 6 bits and 5120 x 34816 at 5 bits, m = 256 to 4096).  A
+  // 256-column CTA pays off only when decoding is cheap (mul1); with the
+  // costlier decoders its two-stage pipeline leaves the tensor core waiting.
   bool edges256 = (a.n % 256) == 0;
   for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
-  return edges256 ? TcShape::kN256R2 : TcShape::kN128R2;
+  const int64_t g128 = (a.m + 127) / 128, g256 = (a.m + 255) / 256;
+  const double t128 = large_batch_time(a.n / 128 * g128, kCost128);
+  const double t128r2 = large_batch_time(a.n / 128 * g256, 1.0);
+  const double t256r2 = edges256 ? large_batch_time(a.n / 256 * g256, cb == 2 ? kCost256Mul1 : kCost256) : 1e300;
+  if (t128r2 <= t128 && t128r2 <= t256r2) return TcShape::kN128R2;
+  return t256r2 < t128 ? TcShape::kN256R2 : TcShape::kN128;
 }
 
 }  // namespace
@@ -116,7 +149,7 @@ TcShape choose_shape(const GemmArgs& a) {
 cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  const TcShape shape = choose_shape(a);
+  const TcShape shape = choose_shape(a, cb);
   const ShapeDims d = dims_of(shape);
   // rows per activation copy: every allocated row when a stage holds several
   // atoms (their regions sit back to back), else just the rows in use
