@@ -7,17 +7,28 @@
 // BN < 128 a thread-block cluster of 128/BN CTAs spans one 128-column Hadamard
 // block: each CTA accumulates its own columns and the epilogue reads the
 // partners' fp32 tiles through distributed shared memory, so the arithmetic is
-// the same whatever BN is.
+// the same whatever BN is.  With PAIR = 2 two CTAs that own the same columns and
+// neighbouring rows form a cluster: each decodes half of the columns and copies
+// its half of the decoded operand into the partner's shared memory, so every
+// decoded weight feeds 2*RG*128 rows.
+//
+// Shared memory holds three rings, each with its own depth: rotated
+// activations (NX slots, RG row groups of KA swizzle atoms of 64 k), decoded
+// weights (NW slots, the tensor core's B operand) and trellis words (NT slots).
+// The trellis ring is deep, so the copies of the compressed weights run far
+// ahead of the decoders, and activation copies never wait for a decode.
 //
 // Warp roles:
-//   warp 0      TMA producer: per stage (KA swizzle atoms of 64 k), one 3-D
-//               tensor copy of the CTA's trellis tiles for the stage's k16 rows
-//               and one 4-D tensor copy of the rotated activations xh (KA
-//               atoms, 128-byte swizzle) per row group, all completing on full[s];
+//   warp 0      trellis producer: one 3-D tensor copy per stage of the CTA's
+//               tiles for the stage's k16 rows;
 //   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma
 //               kind::f16 (M=128, N=BN, K=16) per row group and k16 step, fp32
 //               accumulators in tensor memory;
-//   warps 2..17 decoders: each lane decodes its 8 values of a 16x16 tile
+//   warp 2      activation producer: one 4-D tensor copy of xh (KA atoms,
+//               128-byte swizzle) per row group and stage;
+//   warp 3      with PAIR = 2, sends the CTA's decoded half of each stage to
+//               the partner (bulk copy into its shared memory);
+//   warps 4..19 decoders: each lane decodes its 8 values of a 16x16 tile
 //               (bitshift trellis + procedural codebook, TensorFold PR #740,
 //               "Arithmetic" step 2) into registers in mma B-fragment order and
 //               stmatrix stores them into the 128-byte-swizzled K-major B
@@ -25,13 +36,14 @@
 //
 // Small batches: the activation region of an atom holds only XR rows.  The
 // tensor core still reads 128 rows; rows past XR land on later bytes of the
-// same stage (decoded weights, trellis words), which only feed accumulator
-// rows that are never stored.  The read span always stays inside the stage.
+// rings, which only feed accumulator rows that are never stored.  The read
+// span always stays inside the rings.
 //
-// Each tile is decoded exactly once per CTA.  The fp32 sum over k is a fixed
-// sequence of tcgen05 k16 steps in ascending k for every row, whatever m or the
-// tiling, so rows are byte-equal across batch sizes.  Every wait is bounded: a
-// kernel that gives up records kErrWaitTimeout and skips its stores.
+// Each tile is decoded exactly once per CTA (per pair with PAIR = 2).  The fp32
+// sum over k is a fixed sequence of tcgen05 k16 steps in ascending k for every
+// row, whatever m or the tiling, so rows are byte-equal across batch sizes.
+// Every wait is bounded: a kernel that gives up records kErrWaitTimeout and
+// skips its stores.
 #pragma once
 
 #include "exl3_device.cuh"
@@ -41,44 +53,64 @@
 namespace exl3 {
 
 constexpr int kTcDecodeWarps = 16;  // decoder / epilogue warps
-constexpr int kTcThreads = 32 * (2 + kTcDecodeWarps);
+constexpr int kTcFirstDecoder = 4;  // warps 0..3: trellis producer, MMA issuer, activation producer, sender
+constexpr int kTcThreads = 32 * (kTcFirstDecoder + kTcDecodeWarps);
 constexpr int kTcSmemBudget = 227 * 1024;
 
-template <int BITS, int BN, int RG, int KA, int XR>
+template <int BITS, int BN, int RG, int KA, int XR, int PAIR>
 struct TcCfg {
-  static constexpr int kCluster = BN < 128 ? 128 / BN : 1;
-  static constexpr int kXAtom = XR * 128;                        // one atom of one row group
-  static constexpr int kXBytes = RG * KA * kXAtom;
-  static constexpr int kWAtom = BN * 128;                        // decoded B operand, one atom
-  static constexpr int kWBytes = KA * kWAtom;
-  static constexpr int kTrRowBytes = (BN / 16) * 32 * BITS;      // one k16 row of BN/16 tiles
-  static constexpr int kTrRows = 4 * KA;
-  static constexpr int kTrBytes = kTrRows * kTrRowBytes;
-  static constexpr int kStageBytes = ((kXBytes + kWBytes + kTrBytes) + 1023) / 1024 * 1024;
+  static constexpr int kClusterX = BN < 128 ? 128 / BN : 1;  // CTAs spanning a Hadamard block
+  static constexpr int kCluster = kClusterX * PAIR;
+  static constexpr int kXAtom = XR * 128;                     // one atom of one row group
+  static constexpr int kXSlot = RG * KA * kXAtom;             // activations of a stage
+  static constexpr int kWAtom = BN * 128;                     // decoded B operand, one atom
+  static constexpr int kWSlot = KA * kWAtom;                  // decoded operand of a stage
+  static constexpr int kBNL = BN / PAIR;                      // columns this CTA decodes
+  static constexpr int kWHalfAtom = kBNL * 128;               // its rows of one atom
+  static constexpr int kTrRows = 4 * KA;                      // k16 rows per stage
+  static constexpr int kTrCopy = kTrRows * (kBNL / 16) * 32 * BITS;  // bytes of one trellis copy
+  static constexpr int kTSlot = (kTrCopy + 127) / 128 * 128;
   static constexpr int kCtrlBytes = 1024;
-  static constexpr int kStages0 = (kTcSmemBudget - 1024 - kCtrlBytes) / kStageBytes;
-  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
-  static constexpr int kSmem = 1024 + kCtrlBytes + kStages * kStageBytes;
+  static constexpr int kAvail = kTcSmemBudget - 1024 - kCtrlBytes;
+  // Ring depths: three decoded-operand slots when two activation slots and
+  // four trellis slots still fit, else two; then four activation slots for
+  // small batches (they are small), otherwise three if four trellis slots
+  // still fit, else two; the trellis ring takes the rest.
+  static constexpr int kNW = (kAvail - 2 * kXSlot - 3 * kWSlot >= 4 * kTSlot) ? 3 : 2;
+  static constexpr int kNX = XR < 128 ? 4 : (kAvail - 3 * kXSlot - kNW * kWSlot >= 4 * kTSlot) ? 3 : 2;
+  static constexpr int kNT0 = (kAvail - kNX * kXSlot - kNW * kWSlot) / kTSlot;
+  static constexpr int kNT = kNT0 > 16 ? 16 : kNT0;
+  static constexpr int kXRing = 0;  // byte offsets of the rings
+  static constexpr int kWRing = kNX * kXSlot;
+  static constexpr int kTRing = kWRing + kNW * kWSlot;
+  static constexpr int kRingBytes = kTRing + kNT * kTSlot;
+  static constexpr int kSmem = 1024 + kCtrlBytes + kRingBytes;
   static constexpr int kTmemCols =
       RG * BN <= 32 ? 32 : RG * BN <= 64 ? 64 : RG * BN <= 128 ? 128 : RG * BN <= 256 ? 256 : 512;
-  static constexpr int kTiles = kTrRows * (BN / 16);    // tiles decoded per stage
+  static constexpr int kTiles = kTrRows * (kBNL / 16);  // tiles decoded per stage
   static constexpr int kTpw = kTiles / kTcDecodeWarps;  // per decoder warp
   static constexpr int kZStride = BN + 4;               // epilogue staging row stride (floats)
   static_assert(RG * BN <= 512, "accumulators exceed tensor memory");
-  static_assert(kStages >= 2, "not enough shared memory for two stages");
-  static_assert(kTiles % kTcDecodeWarps == 0, "tiles per stage must split evenly over the decoders");
+  static_assert(kNT >= 4, "not enough shared memory for four trellis slots");
+  static_assert(kTiles % kTcDecodeWarps == 0 && kTpw >= 1, "tiles per stage must split evenly over the decoders");
   static_assert(XR == 128 || RG == 1, "partial activation regions need a single row group");
-  static_assert(XR == 128 || (KA - 1) * kXAtom + 16384 <= kStageBytes,
-                "the tensor core's 128-row read of the last atom must stay inside the stage");
-  static_assert(128 * kZStride * 4 <= kStages * kStageBytes, "epilogue tile must fit in the stage buffers");
+  static_assert(kXSlot % 1024 == 0 && kWSlot % 1024 == 0, "operand slots must keep 1024-byte swizzle alignment");
+  static_assert(XR == 128 || kWRing - kXAtom + 16384 <= kRingBytes,
+                "the tensor core's 128-row read of the last atom must stay inside the rings");
+  static_assert(PAIR == 1 || (BN >= 128 && XR == 128), "pairs share whole 128-column blocks of full row groups");
+  static_assert(kWHalfAtom % 1024 == 0, "each CTA's half of an atom must be whole 8-row swizzle groups");
+  static_assert(128 * kZStride * 4 <= kRingBytes, "epilogue tile must fit in the rings");
+  static_assert((2 * kNT + 2 * kNX + 3 * kNW + 1) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
-  using C = TcCfg<BITS, BN, RG, KA, XR>;
-  constexpr int ST = C::kStages;
-  constexpr int CL = C::kCluster;
+  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
+  constexpr int NT = C::kNT;
+  constexpr int NX = C::kNX;
+  constexpr int NW = C::kNW;
+  constexpr int CLX = C::kClusterX;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
   const GemmArgs& a = p.a;
 
@@ -87,19 +119,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // the compiler keeps every access in the shared address space (an integer
   // round trip would turn the window loads into generic loads).
   uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(base);
-  uint64_t* wfull = full + ST;
-  uint64_t* empty = wfull + ST;
-  uint64_t* accfull = empty + ST;
+  uint64_t* tfull = reinterpret_cast<uint64_t*>(base);  // trellis slot landed (TMA bytes)
+  uint64_t* tempty = tfull + NT;                        // trellis slot decoded by every decoder warp
+  uint64_t* xfull = tempty + NT;                        // activation slot landed (TMA bytes)
+  uint64_t* xempty = xfull + NX;                        // activation slot consumed by the MMA
+  uint64_t* wfull = xempty + NX;                        // decoded operand complete
+  uint64_t* wdone = wfull + NW;                         // this CTA's decoders done (PAIR = 2)
+  uint64_t* wempty = wdone + NW;                        // decoded operand consumed by the MMA(s)
+  uint64_t* accfull = wempty + NW;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accfull + 1);
   volatile uint32_t* failed = tmem_slot + 1;  // set by the MMA issuer if any wait gave up
-  uint8_t* stages = base + C::kCtrlBytes;
+  uint8_t* rings = base + C::kCtrlBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t c0 = (int64_t)blockIdx.x * BN;
   const int64_t row0 = (int64_t)blockIdx.y * (128 * RG);
   const int part = (int)blockIdx.z;
+  // rank within the pair (cluster dims {1, 2, 1})
+  const uint32_t prank = PAIR > 1 ? cluster_ctarank() : 0u;
   // this CTA's k range in 64-wide atoms: whole 128-row blocks of k per part
   const int64_t kb0 = (int64_t)part * (a.k >> 7) / a.parts * 2;
   const int64_t kb1 = (int64_t)(part + 1) * (a.k >> 7) / a.parts * 2;
@@ -111,10 +149,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (i < a.num_shards && c0 >= a.shard_cols[i]) shard = i;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&wfull[s], kTcDecodeWarps);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < NT; ++s) {
+      mbar_init(&tfull[s], 1);
+      mbar_init(&tempty[s], kTcDecodeWarps);
+    }
+    for (int s = 0; s < NX; ++s) {
+      mbar_init(&xfull[s], 1);
+      mbar_init(&xempty[s], 1);
+    }
+    for (int s = 0; s < NW; ++s) {
+      // PAIR = 2: the sender arrives once and the partner's copy brings its bytes
+      mbar_init(&wfull[s], PAIR > 1 ? 1 : kTcDecodeWarps);
+      mbar_init(&wdone[s], kTcDecodeWarps);
+      mbar_init(&wempty[s], PAIR);  // one commit per MMA issuer of the pair
     }
     mbar_init(accfull, 1);
     *failed = 0u;
@@ -125,29 +172,71 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  // the partner arrives on this CTA's barriers: they must be initialised first
+  if (PAIR > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- trellis producer ----------------
     if (lane == 0) {
-      prefetch_tensormap(&maps.xh);
       prefetch_tensormap(&maps.trellis);
-      const int nt0 = (int)(c0 >> 4);
-      const uint32_t tx = (uint32_t)C::kTrBytes + (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
+      const int nt0 = (int)(c0 >> 4) + (int)prank * (C::kBNL / 16);
       int s = 0;
       uint32_t ph = 0;
       for (int it = 0; it < nk; ++it) {
-        if (!mbar_wait(&empty[s], ph ^ 1u)) break;
-        mbar_arrive_expect_tx(&full[s], tx);
-        uint8_t* st = stages + s * C::kStageBytes;
+        if (!mbar_wait(&tempty[s], ph ^ 1u)) break;
+        mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);  // first 64-wide k atom of the stage
-        tma_tile3d_g2s(st + C::kXBytes + C::kWBytes, &maps.trellis, 0, nt0, atom0 * 4, &full[s]);
+        tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, &tfull[s]);
+        if (++s == NT) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------- activation producer ----------------
+    if (lane == 0) {
+      prefetch_tensormap(&maps.xh);
+      const uint32_t tx = (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int it = 0; it < nk; ++it) {
+        if (!mbar_wait(&xempty[s], ph ^ 1u)) break;
+        mbar_arrive_expect_tx(&xfull[s], tx);
+        const int atom0 = (int)(kb0 + (int64_t)it * KA);
+        uint8_t* o = rings + C::kXRing + s * C::kXSlot;
 #pragma unroll
         for (int r = 0; r < RG; ++r)
-          tma_tile4d_g2s(st + r * KA * C::kXAtom, &maps.xh, 0, (int)(row0 + r * 128), atom0, shard, &full[s]);
-        if (++s == ST) {
+          tma_tile4d_g2s(o + r * KA * C::kXAtom, &maps.xh, 0, (int)(row0 + r * 128), atom0, shard, &xfull[s]);
+        if (++s == NX) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------- sender (pairs) ----------------
+    if (PAIR > 1 && lane == 0) {
+      const uint32_t wring_u32 = smem_u32(rings + C::kWRing);
+      const uint32_t peer = prank ^ 1u;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int it = 0; it < nk; ++it) {
+        if (!mbar_wait(&wdone[s], ph)) break;
+        // this CTA's half is complete: expect the partner's half and send ours
+        mbar_arrive_expect_tx(&wfull[s], (uint32_t)(KA * C::kWHalfAtom));
+#pragma unroll
+        for (int at = 0; at < KA; ++at) {
+          const uint32_t src = wring_u32 + (uint32_t)(s * C::kWSlot + at * C::kWAtom + (int)prank * C::kWHalfAtom);
+          bulk_s2cluster(mapa_shared(src, peer), src, (uint32_t)C::kWHalfAtom, mapa_shared(smem_u32(&wfull[s]), peer));
+        }
+        if (++s == NW) {
           s = 0;
           ph ^= 1u;
         }
@@ -157,31 +246,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
-      int s = 0;
-      uint32_t ph = 0;
-      const uint64_t desc0 = sdesc_sw128(smem_u32(stages));
+      int xs = 0, ws = 0;
+      uint32_t xph = 0, wph = 0;
+      const uint64_t xdesc0 = sdesc_sw128(smem_u32(rings + C::kXRing));
+      const uint64_t wdesc0 = sdesc_sw128(smem_u32(rings + C::kWRing));
       for (int it = 0; it < nk; ++it) {
-        ok = mbar_wait(&full[s], ph) && mbar_wait(&wfull[s], ph);
+        ok = mbar_wait(&xfull[xs], xph) && mbar_wait(&wfull[ws], wph);
         if (!ok) break;
         tc_fence_after();
         // descriptors of this stage's operands; an operand at byte offset o
-        // from the stage has descriptor da + (o >> 4) (start-address field)
-        const uint64_t da = desc0 + (uint64_t)((s * C::kStageBytes) >> 4);
+        // from a ring has descriptor desc0 + (o >> 4) (start-address field)
+        const uint64_t dx = xdesc0 + (uint64_t)((xs * C::kXSlot) >> 4);
+        const uint64_t dwb = wdesc0 + (uint64_t)((ws * C::kWSlot) >> 4);
 #pragma unroll
         for (int at = 0; at < KA; ++at) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
-              tc_mma_f16(tmem + r * BN, da + (uint64_t)((((r * KA + at) * C::kXAtom) + j * 32) >> 4),
-                         da + (uint64_t)((C::kXBytes + at * C::kWAtom + j * 32) >> 4), kIdesc, (it | at | j) != 0);
+              tc_mma_f16(tmem + r * BN, dx + (uint64_t)((((r * KA + at) * C::kXAtom) + j * 32) >> 4),
+                         dwb + (uint64_t)((at * C::kWAtom + j * 32) >> 4), kIdesc, (it | at | j) != 0);
             }
           }
         }
-        tc_commit(&empty[s]);
-        if (++s == ST) {
-          s = 0;
-          ph ^= 1u;
+        tc_commit(&xempty[xs]);
+        if (PAIR > 1) {
+          tc_commit_multicast(&wempty[ws], (uint16_t)3u);
+        } else {
+          tc_commit(&wempty[ws]);
+        }
+        if (++xs == NX) {
+          xs = 0;
+          xph ^= 1u;
+        }
+        if (++ws == NW) {
+          ws = 0;
+          wph ^= 1u;
         }
       }
       if (!ok) *failed = 1u;
@@ -190,7 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncwarp();
   } else {
     // ---------------- decoders ----------------
-    const int dw = warp - 2;
+    const int dw = warp - kTcFirstDecoder;
     const LaneWindow<BITS> lw(lane);
     // the multipliers, copied once from parameter memory into registers
     // (read in place, each use would become a constant-bank load)
@@ -200,7 +300,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Per-warp constant byte offsets, so that a tile costs only its loads, its
     // decode and its store: the lane's three window words inside a tile, and
     // where each of this warp's tiles lands in the decoded operand.
-    constexpr int kTilesN = BN / 16;
+    constexpr int kTilesN = C::kBNL / 16;
     constexpr int kTileBytes = 32 * BITS;
     const uint32_t word_off[3] = {dw * (uint32_t)kTileBytes + 4u * lw.idx[0], dw * (uint32_t)kTileBytes + 4u * lw.idx[1],
                                   dw * (uint32_t)kTileBytes + 4u * lw.idx[2]};
@@ -212,19 +312,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int i = 0; i < C::kTpw; ++i) {
         const int t = dw + i * kTcDecodeWarps;
         const int kt_l = t / kTilesN;  // k16 row within the stage
-        const int row = (t - kt_l * kTilesN) * 16 + row_in;
+        const int row = (int)prank * C::kBNL + (t - kt_l * kTilesN) * 16 + row_in;
         const int chunk = 2 * (kt_l & 3) + chunk_hi;
         w_off[i] = (uint32_t)((kt_l >> 2) * C::kWAtom + row * 128 + ((chunk ^ (row & 7)) << 4));
       }
     }
-    const uint32_t stages_u32 = smem_u32(stages);
-    int s = 0;
-    uint32_t ph = 0;
+    const uint32_t tring_u32 = smem_u32(rings + C::kTRing);
+    const uint32_t wring_u32 = smem_u32(rings + C::kWRing);
+    uint64_t* const wready = PAIR > 1 ? wdone : wfull;
+    int ts = 0, ws = 0;
+    uint32_t tph = 0, wph = 0;
     for (int it = 0; it < nk; ++it) {
-      if (!mbar_wait(&full[s], ph)) break;
-      const uint32_t st = stages_u32 + (uint32_t)(s * C::kStageBytes);
-      const uint32_t trbase = st + C::kXBytes + C::kWBytes;
-      const uint32_t wbase = st + C::kXBytes;
+      if (!mbar_wait(&tfull[ts], tph)) break;
+      const uint32_t trbase = tring_u32 + (uint32_t)(ts * C::kTSlot);
       // all window words of this warp's tiles first, so their latency overlaps
       uint32_t wv[C::kTpw][3];
 #pragma unroll
@@ -234,6 +334,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         wv[i][1] = ld_shared_u32(trbase + word_off[1] + i * kStep);
         wv[i][2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2] + i * kStep) : 0u;
       }
+      // the decoded-operand slot must have been consumed by the MMA(s) of its last use
+      if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+      const uint32_t wbase = wring_u32 + (uint32_t)(ws * C::kWSlot);
 #pragma unroll
       for (int i = 0; i < C::kTpw; ++i) {
         const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
@@ -243,10 +346,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&wfull[s]);
-      if (++s == ST) {
-        s = 0;
-        ph ^= 1u;
+      if (lane == 0) {
+        mbar_arrive(&wready[ws]);
+        // The decode above consumed every window word, so the loads have
+        // returned: the trellis slot can go back to the producer.  (An arrive
+        // issued right after the loads, before their values are used, let the
+        // next copy overwrite words that were still being read.)
+        mbar_arrive(&tempty[ts]);
+      }
+      if (++ts == NT) {
+        ts = 0;
+        tph ^= 1u;
+      }
+      if (++ws == NW) {
+        ws = 0;
+        wph ^= 1u;
       }
     }
   }
@@ -254,20 +368,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---------------- epilogue ----------------
   // Decoder warps wait for the accumulators; every warp takes part in the
   // block / cluster barriers below.
-  const int dw = warp - 2;
+  const int dw = warp - kTcFirstDecoder;
   bool ok = true;
-  if (warp >= 2) {
+  if (warp >= kTcFirstDecoder) {
     ok = mbar_wait(accfull, 0) && *failed == 0u;
+    if (PAIR > 1) {
+      // This CTA's copies of its decoded halves into the partner read the
+      // operand ring, which the epilogue below overwrites: they are complete
+      // once the partner's MMAs have consumed them, i.e. when every slot's
+      // final phase (which also takes the partner's commit) has completed.
+      // That also retires the partner's last arrivals on this CTA's barriers.
+      if (lane < NW && lane < nk) {
+        const int uses = (nk - lane + NW - 1) / NW;
+        ok = mbar_wait(&wempty[lane], (uint32_t)(uses - 1) & 1u) && ok;
+      }
+      ok = __all_sync(0xFFFFFFFFu, ok);
+    }
     tc_fence_after();
   }
   const bool bf16 = a.y_bf16 != 0;
   uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
-  float* zs = reinterpret_cast<float*>(stages);
+  float* zs = reinterpret_cast<float*>(rings);
   constexpr int kZ = C::kZStride;
 
   if (a.parts > 1) {
     // split-k: this part's fp32 sums go straight to acc[part][row][col]
-    if (warp >= 2) {
+    if (warp >= kTcFirstDecoder) {
       const int quarter = warp & 3;
       float* dst = a.acc + (int64_t)part * a.m * a.n;
       for (int r = 0; r < RG; ++r) {
@@ -287,12 +413,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
-    const uint32_t rank = (CL > 1) ? cluster_ctarank() : 0u;
+    const uint32_t rank = (CLX > 1) ? cluster_ctarank() : 0u;
     const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
     constexpr int kSpan = BN < 128 ? 128 : BN;
     for (int r = 0; r < RG; ++r) {
       // 1. tensor memory -> this CTA's fp32 tile zs[128][BN]
-      if (warp >= 2) {
+      if (warp >= kTcFirstDecoder) {
         const int quarter = warp & 3;
         for (int cc = dw >> 2; cc < BN / 32; cc += kTcDecodeWarps / 4) {
           uint32_t q[32];
@@ -305,13 +431,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                               __uint_as_float(q[i + 2]), __uint_as_float(q[i + 3]));
         }
       }
-      if (CL > 1) {
+      if (CLX > 1) {
         cluster_sync();
       } else {
         __syncthreads();
       }
       // 2. rows: lane l owns columns 4l..4l+3 of each 128-column block of the span
-      if (warp >= 2) {
+      if (warp >= kTcFirstDecoder) {
         for (int hb = 0; hb < kSpan / 128; ++hb) {
           const int span_col = hb * 128 + 4 * lane;
           const uint32_t src_rank = (uint32_t)(span_col / BN);
@@ -322,12 +448,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 __half2float(__ushort_as_half((uint16_t)(sv.x >> 16))),
                                 __half2float(__ushort_as_half((uint16_t)(sv.y & 0xFFFF))),
                                 __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)))};
-          const uint32_t zsrc = (CL > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs);
-          for (int rr = (int)rank + CL * dw; rr < 128; rr += CL * kTcDecodeWarps) {
+          const uint32_t zsrc = (CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs);
+          for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
             const int64_t row = row0 + r * 128 + rr;
             if (!ok || row >= a.m) break;  // rows ascend with rr
             float4 z4;
-            if (CL > 1) {
+            if (CLX > 1) {
               z4 = ld_shared_cluster_f4(zsrc + (uint32_t)((rr * kZ + local_col) * 4));
             } else {
               z4 = *reinterpret_cast<const float4*>(zs + rr * kZ + local_col);
@@ -345,7 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       // the tile is reused by the next row group, and partners may still read it
-      if (CL > 1) {
+      if (CLX > 1) {
         cluster_sync();
       } else {
         __syncthreads();
@@ -354,14 +480,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (C::kCluster > 1) {
+    cluster_sync();
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1>
 cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
-  using C = TcCfg<BITS, BN, RG, KA, XR>;
-  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR>;
+  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
+  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR>;
   static bool configured = false;  // benign race: every thread sets the same attribute
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
@@ -369,14 +499,16 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
     configured = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.a.n / BN), (unsigned)((p.a.m + 128 * RG - 1) / (128 * RG)), (unsigned)p.a.parts);
+  // a pair's second CTA may own only rows past m: it still decodes its half
+  const int64_t row_blocks = (p.a.m + 128 * RG - 1) / (128 * RG);
+  cfg.gridDim = dim3((unsigned)(p.a.n / BN), (unsigned)((row_blocks + PAIR - 1) / PAIR * PAIR), (unsigned)p.a.parts);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C::kCluster;
-  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.x = C::kClusterX;
+  attr[0].val.clusterDim.y = PAIR;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -390,8 +522,10 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN32Small: return launch_tc_variant<BITS, CB, 32, 1, 4, 32>(maps, p, stream);
     case TcShape::kN64Small: return launch_tc_variant<BITS, CB, 64, 1, 2, 32>(maps, p, stream);
     case TcShape::kN128Small: return launch_tc_variant<BITS, CB, 128, 1, 2, 32>(maps, p, stream);
-    case TcShape::kN128: return launch_tc_variant<BITS, CB, 128, 1, 1, 128>(maps, p, stream);
+    case TcShape::kN128: return launch_tc_variant<BITS, CB, 128, 1, 2, 128>(maps, p, stream);
     case TcShape::kN128R2: return launch_tc_variant<BITS, CB, 128, 2, 1, 128>(maps, p, stream);
+    case TcShape::kN128R2P: return launch_tc_variant<BITS, CB, 128, 2, 1, 128, 2>(maps, p, stream);
+    case TcShape::kN256R2P: return launch_tc_variant<BITS, CB, 256, 2, 1, 128, 2>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <stdlib.h>
 
 #include "exl3_launch.h"
 
@@ -47,7 +48,8 @@ cudaError_t make_xh_map(CUtensorMap* map, const uint16_t* xh, int64_t m, int64_t
 }
 
 // trellis is int16 [k/16][n/16][16*bits], viewed as 3-D {16*bits, n/16, k/16}; one
-// copy brings a CTA's bn/16 tiles for rows k16 of a stage, stored row after row.
+// copy brings the bn/16 tiles a CTA decodes for the k16 rows of a stage, stored
+// row after row.
 cudaError_t make_trellis_map(CUtensorMap* map, const int16_t* trellis, int64_t k, int64_t n, int bits, int bn,
                              int rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
@@ -63,17 +65,19 @@ cudaError_t make_trellis_map(CUtensorMap* map, const int16_t* trellis, int64_t k
 }
 
 struct ShapeDims {
-  int bn, ka, xr;
+  int bn, ka, xr, pair;
 };
 
 ShapeDims dims_of(TcShape s) {
   switch (s) {
-    case TcShape::kN32Small: return {32, 4, 32};
-    case TcShape::kN64Small: return {64, 2, 32};
-    case TcShape::kN128Small: return {128, 2, 32};
-    case TcShape::kN128: return {128, 1, 128};
-    case TcShape::kN128R2: return {128, 1, 128};
-    default: return {256, 1, 128};
+    case TcShape::kN32Small: return {32, 4, 32, 1};
+    case TcShape::kN64Small: return {64, 2, 32, 1};
+    case TcShape::kN128Small: return {128, 2, 32, 1};
+    case TcShape::kN128: return {128, 2, 128, 1};
+    case TcShape::kN128R2: return {128, 1, 128, 1};
+    case TcShape::kN128R2P: return {128, 1, 128, 2};
+    case TcShape::kN256R2P: return {256, 1, 128, 2};
+    default: return {256, 1, 128, 1};
   }
 }
 
@@ -87,7 +91,7 @@ ShapeDims dims_of(TcShape s) {
 // tensor core's 128-row operand reads.
 constexpr double kRel64 = 0.48, kRel32 = 0.43;
 
-constexpr double kCost128 = 0.79, kCost256 = 2.26, kCost256Mul1 = 1.72;
+constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33;
 
 // SMs of the current device, read once per device.
 int64_t sm_count() {
@@ -117,8 +121,8 @@ double large_batch_time(int64_t ctas, double cost) {
   return (double)((ctas + sms - 1) / sms) * cost;
 }
 
-TcShape choose_shape(const GemmArgs& a, int cb) {
-  if (a.parts > 1) return a.m <= 32 ? TcShape::kN128Small : (a.m <= 128 ? TcShape::kN128 : TcShape::kN128R2);
+TcShape choose_shape(const GemmArgs& a) {
+  if (a.parts > 1 && a.m <= 128) return a.m <= 32 ? TcShape::kN128Small : TcShape::kN128;
   if (a.m <= 32) {
     // pick the column width whose grid keeps the most decode throughput busy
     const double r128 = small_batch_rate(a.n / 128, 1.0);
@@ -131,17 +135,29 @@ TcShape choose_shape(const GemmArgs& a, int cb) {
   if (a.m <= 128) return TcShape::kN128;
   // Larger batches: least estimated time over whole waves.  Per-CTA costs are
   // relative to a 256-row, 128-column CTA over the same k, measured on GB300
-  // (5120 x 12288 at 6 bits and 5120 x 34816 at 5 bits, m = 256 to 4096).  A
-  // 256-column CTA pays off only when decoding is cheap (mul1); with the
-  // costlier decoders its two-stage pipeline leaves the tensor core waiting.
+  // (5120 x 12288 at 6 bits, 5120 x 34816 at 5 bits, 12288 x 4096 at 5 bits,
+  // m = 256 to 4096).  Pair shapes decode half of the columns per CTA; their
+  // grid pads the row blocks to an even count.
   bool edges256 = (a.n % 256) == 0;
   for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
-  const int64_t g128 = (a.m + 127) / 128, g256 = (a.m + 255) / 256;
-  const double t128 = large_batch_time(a.n / 128 * g128, kCost128);
-  const double t128r2 = large_batch_time(a.n / 128 * g256, 1.0);
-  const double t256r2 = edges256 ? large_batch_time(a.n / 256 * g256, cb == 2 ? kCost256Mul1 : kCost256) : 1e300;
-  if (t128r2 <= t128 && t128r2 <= t256r2) return TcShape::kN128R2;
-  return t256r2 < t128 ? TcShape::kN256R2 : TcShape::kN128;
+  // split-k parts multiply every grid
+  const int64_t g128 = (a.m + 127) / 128 * a.parts, g256 = (a.m + 255) / 256 * a.parts,
+                g512 = 2 * ((a.m + 511) / 512) * a.parts;
+  struct Option {
+    TcShape shape;
+    double time;
+  };
+  const Option opts[5] = {
+      {TcShape::kN128R2, large_batch_time(a.n / 128 * g256, 1.0)},
+      {TcShape::kN128, large_batch_time(a.n / 128 * g128, kCost128)},
+      {TcShape::kN128R2P, large_batch_time(a.n / 128 * g512, kCost128P)},
+      {TcShape::kN256R2, edges256 ? large_batch_time(a.n / 256 * g256, kCost256) : 1e300},
+      {TcShape::kN256R2P, edges256 ? large_batch_time(a.n / 256 * g512, kCost256P) : 1e300},
+  };
+  Option best = opts[0];
+  for (const Option& o : opts)
+    if (o.time < best.time) best = o;
+  return best.shape;
 }
 
 }  // namespace
@@ -149,7 +165,8 @@ TcShape choose_shape(const GemmArgs& a, int cb) {
 cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  const TcShape shape = choose_shape(a, cb);
+  TcShape shape = choose_shape(a);
+  if (const char* f = getenv("EXL3_FORCE_SHAPE")) shape = (TcShape)atoi(f);
   const ShapeDims d = dims_of(shape);
   // rows per activation copy: every allocated row when a stage holds several
   // atoms (their regions sit back to back), else just the rows in use
@@ -157,7 +174,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
   TcMaps maps;
   cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, d.ka);
   if (e != cudaSuccess) return e;
-  e = make_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, d.bn, 4 * d.ka);
+  e = make_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, d.bn / d.pair, 4 * d.ka);
   if (e != cudaSuccess) return e;
   switch (bits) {
     case 1: return launch_gemm_tc_bits<1>(maps, p, cb, shape, stream);
