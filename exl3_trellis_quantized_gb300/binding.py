@@ -51,6 +51,8 @@ def lib() -> ctypes.CDLL:
     L.exl3_splitk_parts.restype = i32
     L.exl3_splitk_workspace_bytes.argtypes = [i64, i64, i64]
     L.exl3_splitk_workspace_bytes.restype = sz
+    L.exl3_test_gemm_shape.argtypes = [i32] + L.exl3_gemm.argtypes[:-1] + [vp, sz, vp]
+    L.exl3_test_gemm_shape.restype = ctypes.c_int
     L.exl3_test_codebook.argtypes = [ctypes.c_int, vp, vp]
     L.exl3_test_unpack.argtypes = [vp, i32, ctypes.c_int, i64, i64, vp, vp]
     L.exl3_status_string.argtypes = [ctypes.c_int]
@@ -199,6 +201,30 @@ def linear(x: torch.Tensor, trellis: torch.Tensor, bits: int, cb, suh: torch.Ten
     if acc is not None:
         return gemm_splitk(xh, trellis, bits, cb, svh, shard_cols, acc, out_dtype, out)
     return gemm(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+
+
+# Tile shapes exl3_test_gemm_shape accepts (EXL3_TEST_TILE_SHAPES in include/exl3.h).
+TEST_TILE_SHAPES = 8
+
+
+def test_gemm_shape(tile_shape: int, xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor,
+                    shard_cols: Sequence[int], acc: Optional[torch.Tensor] = None, out_dtype=torch.bfloat16,
+                    out: Optional[torch.Tensor] = None) -> Optional[torch.Tensor]:
+    """exl3_gemm (or the split-k GEMM when ``acc`` is given) with a fixed tile shape.
+
+    Returns None, launching nothing, when the shape cannot run the call.
+    """
+    m, k, n, cols, ns, cbid, out = _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
+    if acc is not None:
+        _need(acc, torch.float32, "acc")
+    st = lib().exl3_test_gemm_shape(int(tile_shape), _ptr(xh), m, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns,
+                                    _ptr(out), _BF16 if out.dtype == torch.bfloat16 else _F16, n,
+                                    _ptr(acc) if acc is not None else None, acc.numel() * 4 if acc is not None else 0,
+                                    _stream(xh))
+    if st == 2:
+        return None
+    _check(st, "exl3_test_gemm_shape")
+    return out
 
 
 def test_codebook(cb, device="cuda") -> torch.Tensor:

@@ -128,20 +128,34 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
                                exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols,
                                int32_t num_shards, void* y, exl3_dtype_t y_dtype, int64_t n, float* acc,
                                size_t acc_bytes, void* stream) {
+  return exl3_test_gemm_shape(-1, xh, m, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, acc,
+                              acc_bytes, stream);
+}
+
+exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
+                                   const int16_t* trellis, int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
+                                   const int32_t* shard_cols, int32_t num_shards, void* y, exl3_dtype_t y_dtype,
+                                   int64_t n, float* acc, size_t acc_bytes, void* stream) {
+  // tile_shape -1 (only from exl3_gemm_splitk): the library's own choice
+  const bool split = acc != nullptr || tile_shape < 0;
   exl3::GemmArgs a;
   exl3_status_t st = check_gemm(xh, m, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
   if (st != EXL3_OK) return st;
+  if (tile_shape < -1 || tile_shape >= EXL3_TEST_TILE_SHAPES) return EXL3_EINVAL;
+  if (split) {
+    if (m > 0 && !aligned16(acc)) return EXL3_EINVAL;
+    if (acc_bytes < exl3_splitk_workspace_bytes(m, k, n)) return EXL3_EWORKSPACE;
+    a.acc = acc;
+    a.parts = exl3_splitk_parts(k, n);
+  }
+  if (tile_shape >= 0 && !exl3::tc_shape_supported(tile_shape, a)) return EXL3_EUNSUPPORTED;
   if (m == 0) return EXL3_OK;
-  if (!aligned16(acc)) return EXL3_EINVAL;
-  if (acc_bytes < exl3_splitk_workspace_bytes(m, k, n)) return EXL3_EWORKSPACE;
-  a.acc = acc;
-  a.parts = exl3_splitk_parts(k, n);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.parts == 1) {
-    // one part: the fused epilogue already does everything; acc stays zero
-    return cuda_status(exl3::launch_gemm_tc(a, bits, cb, s), "exl3_gemm_splitk");
+    // no split (or one part: the fused epilogue does everything; acc stays zero)
+    return cuda_status(exl3::launch_gemm_tc(a, bits, cb, s, tile_shape), "exl3_gemm");
   }
-  st = cuda_status(exl3::launch_gemm_tc(a, bits, cb, s), "exl3_gemm_splitk parts");
+  st = cuda_status(exl3::launch_gemm_tc(a, bits, cb, s, tile_shape), "exl3_gemm_splitk parts");
   if (st != EXL3_OK) return st;
   return cuda_status(exl3::launch_splitk_epilogue(a, s), "exl3_gemm_splitk epilogue");
 }

@@ -73,7 +73,11 @@ enum class TcShape : int {
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.
-cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream);
+// shape < 0: chosen from the sizes; otherwise a TcShape value that
+// tc_shape_supported() accepted.
+cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream, int shape = -1);
+// Whether tile shape `shape` can run the call described by `args`.
+bool tc_shape_supported(int shape, const GemmArgs& args);
 template <int BITS>
 cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, TcShape shape,
                                 cudaStream_t stream);

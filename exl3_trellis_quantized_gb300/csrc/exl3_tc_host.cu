@@ -4,7 +4,6 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
-#include <stdlib.h>
 
 #include "exl3_launch.h"
 
@@ -162,11 +161,24 @@ TcShape choose_shape(const GemmArgs& a) {
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
+bool tc_shape_supported(int shape, const GemmArgs& a) {
+  if (shape < 0 || shape > (int)TcShape::kN256R2P) return false;
+  const TcShape s = (TcShape)shape;
+  const ShapeDims d = dims_of(s);
+  if (d.xr < 128 && a.m > d.xr) return false;  // small-batch shapes hold XR rows
+  if (d.ka == 4 && ((a.k / 128) % 2 != 0 || a.parts > 1)) return false;
+  if (d.bn == 256) {
+    if (a.n % 256 != 0) return false;
+    for (int i = 0; i <= a.num_shards; ++i)
+      if (a.shard_cols[i] % 256 != 0) return false;
+  }
+  return true;
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream, int forced) {
   TcParams p;
   p.a = a;
-  TcShape shape = choose_shape(a);
-  if (const char* f = getenv("EXL3_FORCE_SHAPE")) shape = (TcShape)atoi(f);
+  const TcShape shape = forced >= 0 ? (TcShape)forced : choose_shape(a);
   const ShapeDims d = dims_of(shape);
   // rows per activation copy: every allocated row when a stage holds several
   // atoms (their regions sit back to back), else just the rows in use

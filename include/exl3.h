@@ -169,6 +169,29 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
                                int64_t k, int64_t n, uint16_t* wq, void* stream);
 
 /*
+ * exl3_test_gemm_shape: exl3_gemm (acc == NULL) or exl3_gemm_splitk (acc !=
+ * NULL, same workspace rules) with the kernel's tile shape fixed by the caller
+ * instead of chosen from the call's sizes.  Every tile shape computes each
+ * output element with the same k16 steps in the same order, so the result must
+ * be byte-equal to the one the library picks; tests use this to check each
+ * shape.  No counterpart in the pages: the tiling is this library's own.
+ *   tile_shape: 0 = 32-column strips (m <= 32, k/128 even, no split-k),
+ *     1 = 64-column strips (m <= 32), 2 = 128 columns (m <= 32),
+ *     3 = 128 columns x 128 rows, 4 = 128 columns x 256 rows,
+ *     5 = 256 columns x 256 rows (n and shard edges multiples of 256),
+ *     6 = pair of 128-column x 256-row CTAs sharing decoded weights,
+ *     7 = pair of 256-column x 256-row CTAs (edges multiples of 256).
+ * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
+ * call (the conditions in parentheses).
+ */
+#define EXL3_TEST_TILE_SHAPES 8
+exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
+                                   const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
+                                   const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
+                                   void* y, exl3_dtype_t y_dtype, int64_t n, float* acc, size_t acc_bytes,
+                                   void* stream);
+
+/*
  * exl3_device_status -- read and clear the library's device-side error flags.
  * Every wait inside the kernels is bounded; a kernel that gives up sets bit 0
  * (EXL3_DEVERR_WAIT_TIMEOUT) and skips its stores instead of hanging.  This call

@@ -14,6 +14,7 @@ import pytest
 import torch
 
 import exl3_trellis_quantized_gb300 as E
+from exl3_trellis_quantized_gb300 import binding as B
 from exl3_trellis_quantized_gb300 import synthetic
 from oracle import exl3_oracle as O
 
@@ -183,6 +184,59 @@ def test_rows_byte_equal_across_tile_shapes(k, n, bits, cb, ms):
     ref = _oracle(x, layer, blocks)
     got = _np(y).reshape(max(ms), n // 128, 128)[:, blocks].reshape(max(ms), -1)
     _assert_columns(got, ref)
+
+
+TILE_CASES = [
+    # k, shard widths, bits, codebook: every tile shape against the library's choice
+    (1024, [512], 3, 1),
+    (2048, [256, 256], 6, 2),
+    (1152, [384, 128], 2, 0),  # an odd number of 128-blocks of k; 128-aligned shard edges
+    (1024, [1024], 8, 1),
+]
+
+
+@pytest.mark.parametrize("k,widths,bits,cb", TILE_CASES,
+                         ids=[f"{c[0]}x{sum(c[1])}b{c[2]}cb{c[3]}" for c in TILE_CASES])
+@pytest.mark.parametrize("split", [False, True], ids=["gemm", "splitk"])
+def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
+    """Each tile shape computes every element with the same k16 steps in the same
+    order, so all of them give the bytes of the library's own choice (and the
+    split-k workspace is left zeroed by each)."""
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=4100 + k + bits)
+    tr, suh, svh = _dev(layer)
+    n = layer.n
+    ran = set()
+    for m in (5, 32, 300, 700):
+        x = synthetic.make_x(m, k, seed=4200 + m).to(DEV)
+        xh = E.input_transform(x, suh)
+        acc = (torch.zeros(max(1, E.splitk_workspace_bytes(m, k, n) // 4), dtype=torch.float32, device=DEV)
+               if split else None)
+        want = (E.gemm_splitk(xh, tr, bits, cb, svh, layer.shard_cols, acc) if split
+                else E.gemm(xh, tr, bits, cb, svh, layer.shard_cols))
+        for shape in range(B.TEST_TILE_SHAPES):
+            got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+            if got is None:
+                continue
+            ran.add(shape)
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"shape {shape} m={m}: bytes differ"
+            if split:
+                assert bool((acc == 0).all()), f"shape {shape} m={m}: workspace not re-zeroed"
+    # the cases reach every shape that their sizes allow
+    need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
+    if not split and (k // 128) % 2 == 0:
+        need.add(0)
+    assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
+
+
+def test_tile_shape_rejections():
+    layer = synthetic.make_layer(1024, [384], 3, 1, seed=4300)
+    tr, suh, svh = _dev(layer)
+    x = synthetic.make_x(40, 1024, seed=4301).to(DEV)
+    xh = E.input_transform(x, suh)
+    assert B.test_gemm_shape(2, xh, tr, 3, 1, svh, layer.shard_cols) is None  # 40 rows > 32
+    assert B.test_gemm_shape(5, xh, tr, 3, 1, svh, layer.shard_cols) is None  # 384 columns: not 256-aligned
+    with pytest.raises(E.Exl3Error):
+        B.test_gemm_shape(8, xh, tr, 3, 1, svh, layer.shard_cols)
 
 
 def test_fused_shards_equal_separate_launches():
