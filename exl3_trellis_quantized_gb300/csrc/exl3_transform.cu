@@ -7,58 +7,150 @@
 // "One op per layer": every shard in one launch, x read once, the bf16 -> fp16
 // conversion folded into the same pass).
 //
-// One warp owns one (row, 128-block); lane l holds elements 4l..4l+3.  x is read
-// once with one 8-byte load per lane and reused for every shard.  The kernel is
-// HBM/L2-bound: 2 bytes in, 2*S bytes out per element.
+// Four lanes own one (row, 128-block): lane q of the four holds elements
+// 32q..32q+31, so a warp covers eight blocks (2 KB of x) per pass with 16-byte
+// loads and stores.  Butterfly stages of stride 1..16 stay in registers; the
+// stride-32 and stride-64 stages exchange with lanes q^1 and q^2.  Each stage
+// computes (a, b) -> (a + b, a - b) on the same pairs as the plain definition,
+// so the order of fp32 adds is the fixed one.  x is read once and reused for
+// every shard.  The kernel is HBM/L2-bound: 2 bytes in, 2*S bytes out per
+// element.
 #include "exl3_device.cuh"
 #include "exl3_launch.h"
 
 namespace exl3 {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 w, uint16_t (&e)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    e[2 * i] = (uint16_t)(u[i] & 0xFFFFu);
+    e[2 * i + 1] = (uint16_t)(u[i] >> 16);
+  }
+}
+
+}  // namespace
+
+template <bool X_BF16>
+__device__ __forceinline__ float to_f32(uint16_t e) {
+  return X_BF16 ? __bfloat162float(__ushort_as_bfloat16(e)) : __half2float(__ushort_as_half(e));
+}
 
 template <bool X_BF16>
 __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
                                                               const uint16_t* __restrict__ suh, int num_shards,
                                                               uint16_t* __restrict__ xh) {
   const int lane = threadIdx.x & 31;
+  const int q = lane & 3;  // which 32 elements of the block
   const int64_t kb = k >> 7;
   const int64_t units = m * kb;
+  const int64_t groups = (units + 7) / 8;  // eight blocks per warp and pass
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < units; u += warps_total) {
-    const int64_t r = u / kb;
-    const int64_t col = (u - r * kb) * 128 + 4 * lane;
-    const uint2 raw = *reinterpret_cast<const uint2*>(x + r * k + col);
-    float xv[4];
-    const uint16_t e[4] = {(uint16_t)(raw.x & 0xFFFF), (uint16_t)(raw.x >> 16), (uint16_t)(raw.y & 0xFFFF),
-                           (uint16_t)(raw.y >> 16)};
+  // element offset of this lane's 32 values in group g (or -1 past the end)
+  auto lane_offset = [&](int64_t g, int64_t* row) -> int64_t {
+    const int64_t u = g * 8 + (lane >> 2);
+    if (g >= groups || u >= units) return -1;
+    *row = u / kb;
+    return *row * k + (u - *row * kb) * 128 + 32 * q;
+  };
+  // x stays packed (bf16 / fp16 pairs) in registers; the next pass's words are
+  // loaded before this pass computes, so two passes of loads are in flight
+  int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int64_t row = 0;
+  int64_t off = lane_offset(g, &row);
+  uint4 cur[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xv[i] = X_BF16 ? __bfloat162float(__ushort_as_bfloat16(e[i])) : __half2float(__ushort_as_half(e[i]));
-    }
+  for (int c = 0; c < 4; ++c) cur[c] = off >= 0 ? *reinterpret_cast<const uint4*>(x + off + 8 * c) : make_uint4(0, 0, 0, 0);
+  for (; g < groups; g += warps_total) {
+    int64_t nrow = 0;
+    const int64_t noff = lane_offset(g + warps_total, &nrow);
+    uint4 nxt[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      nxt[c] = noff >= 0 ? *reinterpret_cast<const uint4*>(x + noff + 8 * c) : make_uint4(0, 0, 0, 0);
+    const int64_t col = off >= 0 ? off - row * k : 32 * q;
     for (int s = 0; s < num_shards; ++s) {
-      const uint2 sr = *reinterpret_cast<const uint2*>(suh + (int64_t)s * k + col);
-      const uint16_t se[4] = {(uint16_t)(sr.x & 0xFFFF), (uint16_t)(sr.x >> 16), (uint16_t)(sr.y & 0xFFFF),
-                              (uint16_t)(sr.y >> 16)};
-      float v[4];
+      float v[32];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) v[i] = xv[i] * __half2float(__ushort_as_half(se[i]));  // exact in fp32
-      fwht128_warp(v, lane);
-      uint16_t o[4];
+      for (int c = 0; c < 4; ++c) {
+        uint16_t e[8], se[8];
+        unpack8(cur[c], e);
+        unpack8(*reinterpret_cast<const uint4*>(suh + (int64_t)s * k + col + 8 * c), se);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = __half_as_ushort(__float2half_rn(v[i] * 0.0625f));  // 2^-4 exact
-      uint2 w;
-      w.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
-      w.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
-      *reinterpret_cast<uint2*>(xh + ((int64_t)s * m + r) * k + col) = w;
+        for (int i = 0; i < 8; ++i) v[8 * c + i] = to_f32<X_BF16>(e[i]) * __half2float(__ushort_as_half(se[i]));  // exact
+      }
+#pragma unroll
+      for (int st = 1; st < 32; st <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if ((i & st) == 0) {
+            const float a = v[i], b = v[i + st];
+            v[i] = a + b;
+            v[i + st] = a - b;
+          }
+        }
+      }
+#pragma unroll
+      for (int st = 1; st <= 2; st <<= 1) {  // element strides 32 and 64
+        const bool upper = (q & st) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p = __shfl_xor_sync(0xffffffffu, v[i], st);
+          v[i] = upper ? (p - v[i]) : (v[i] + p);
+        }
+      }
+      if (off >= 0) {
+        uint16_t* dst = xh + (int64_t)s * m * k + off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint16_t lo = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i] * 0.0625f));  // 2^-4 exact
+            const uint16_t hi = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i + 1] * 0.0625f));
+            w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+          }
+          *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
     }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
+    off = noff;
+    row = nrow;
   }
 }
 
+namespace {
+
+// Blocks that stay resident on the device at once (read once per device and
+// kernel variant): the grid is exactly that, so every warp streams through many
+// passes with the next pass's loads in flight.
+template <bool X_BF16>
+int resident_blocks(int threads) {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152 * 2;
+  if (cache[dev] == 0) {
+    int sms = 0, per_sm = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, input_transform_kernel<X_BF16>, threads, 0);
+    cache[dev] = (sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 1);  // benign race: same value
+  }
+  return cache[dev];
+}
+
+}  // namespace
+
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
                                    int num_shards, uint16_t* xh, cudaStream_t stream) {
-  const int64_t units = m * (k >> 7);
+  const int64_t groups = (m * (k >> 7) + 7) / 8;  // one warp pass each
   const int threads = 256;
-  const int64_t want = (units + 7) / 8;
-  const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  const int64_t want = (groups + 7) / 8;
+  const int cap = x_bf16 ? resident_blocks<true>(threads) : resident_blocks<false>(threads);
+  const int blocks = (int)(want < cap ? want : cap);
   if (x_bf16) {
     input_transform_kernel<true><<<blocks, threads, 0, stream>>>((const uint16_t*)x, m, k, suh, num_shards, xh);
   } else {
