@@ -207,6 +207,22 @@ __device__ __forceinline__ void fwht128_warp(float v[4], int lane) {
   }
 }
 
+// The first five stages (strides 1, 2, 4, 8, 16) of the same butterfly on 32
+// consecutive elements held by one thread.
+__device__ __forceinline__ void fwht32_regs(float (&v)[32]) {
+#pragma unroll
+  for (int st = 1; st < 32; st <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & st) == 0) {
+        const float a = v[i], b = v[i + st];
+        v[i] = a + b;
+        v[i + st] = a - b;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ uint16_t f32_to_out(float v, bool bf16) {
   if (bf16) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
   return __half_as_ushort(__float2half_rn(v));

@@ -417,18 +417,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
     constexpr int kSpan = BN < 128 ? 128 : BN;
     for (int r = 0; r < RG; ++r) {
-      // 1. tensor memory -> this CTA's fp32 tile zs[128][BN]
+      // 1. tensor memory -> zs[128][BN].  Each thread holds one row's 32
+      // consecutive columns after a load and runs the Hadamard stages of
+      // stride 1..16 on them in registers (those pairs never leave a 32-column
+      // chunk), so only the stride-32 and stride-64 stages remain.
       if (warp >= kTcFirstDecoder) {
         const int quarter = warp & 3;
-        for (int cc = dw >> 2; cc < BN / 32; cc += kTcDecodeWarps / 4) {
+        const bool live = row0 + r * 128 + quarter * 32 < a.m;  // this quarter holds stored rows
+        for (int cc = dw >> 2; live && cc < BN / 32; cc += kTcDecodeWarps / 4) {
           uint32_t q[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
           tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(q[e]);
+          fwht32_regs(v);
           float* dst = zs + (quarter * 32 + lane) * kZ + cc * 32;
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + i) = make_float4(__uint_as_float(q[i]), __uint_as_float(q[i + 1]),
-                                                              __uint_as_float(q[i + 2]), __uint_as_float(q[i + 3]));
+          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
       }
       if (CLX > 1) {
@@ -436,37 +442,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else {
         __syncthreads();
       }
-      // 2. rows: lane l owns columns 4l..4l+3 of each 128-column block of the span
+      // 2. rows: lane l owns columns l, l+32, l+64, l+96 of each 128-column
+      // block of the span: the stride-32 and stride-64 stages, then scale and
+      // store (each store instruction writes 32 consecutive columns)
       if (warp >= kTcFirstDecoder) {
         for (int hb = 0; hb < kSpan / 128; ++hb) {
-          const int span_col = hb * 128 + 4 * lane;
-          const uint32_t src_rank = (uint32_t)(span_col / BN);
-          const int local_col = span_col - (int)src_rank * BN;
-          const int64_t col = cbase + span_col;
-          const uint2 sv = *reinterpret_cast<const uint2*>(a.svh + col);
-          const float svf[4] = {__half2float(__ushort_as_half((uint16_t)(sv.x & 0xFFFF))),
-                                __half2float(__ushort_as_half((uint16_t)(sv.x >> 16))),
-                                __half2float(__ushort_as_half((uint16_t)(sv.y & 0xFFFF))),
-                                __half2float(__ushort_as_half((uint16_t)(sv.y >> 16)))};
-          const uint32_t zsrc = (CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs);
+          float svf[4];
+          uint32_t zsrc[4];
+          int64_t col[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int span_col = hb * 128 + lane + 32 * i;
+            const uint32_t src_rank = (uint32_t)(span_col / BN);
+            const int local_col = span_col - (int)src_rank * BN;
+            col[i] = cbase + span_col;
+            svf[i] = __half2float(__ushort_as_half(a.svh[col[i]]));
+            zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
+          }
           for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
             const int64_t row = row0 + r * 128 + rr;
             if (!ok || row >= a.m) break;  // rows ascend with rr
-            float4 z4;
-            if (CLX > 1) {
-              z4 = ld_shared_cluster_f4(zsrc + (uint32_t)((rr * kZ + local_col) * 4));
-            } else {
-              z4 = *reinterpret_cast<const float4*>(zs + rr * kZ + local_col);
-            }
-            float v[4] = {z4.x, z4.y, z4.z, z4.w};
-            fwht128_warp(v, lane);
-            uint16_t o[4];
+            float v[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) o[i] = f32_to_out((v[i] * 0.125f) * svf[i], bf16);
-            uint2 w;
-            w.x = (uint32_t)o[0] | ((uint32_t)o[1] << 16);
-            w.y = (uint32_t)o[2] | ((uint32_t)o[3] << 16);
-            *reinterpret_cast<uint2*>(y + row * a.n + col) = w;
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
+              v[i] = (CLX > 1) ? ld_shared_cluster_f32(addr) : ld_shared_f32(addr);
+            }
+            // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
+            const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+            v[0] = a0 + a2;
+            v[2] = a0 - a2;
+            v[1] = a1 + a3;
+            v[3] = a1 - a3;
+            uint16_t* yr = y + row * a.n;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[i], bf16);
           }
         }
       }
