@@ -296,7 +296,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // (read in place, each use would become a constant-bank load)
     DecodeConsts mc;
 #pragma unroll
-    for (int i = 0; i <= 16; ++i) mc.pow2[i] = a.dc.pow2[i];
+    for (int i = 0; i <= 16; ++i) {
+      // an opaque register copy: the compiler can neither fold the multiply
+      // back into a shift nor re-read the value from constant memory per use
+      uint32_t v = a.dc.pow2[i];
+      asm volatile("" : "+r"(v));
+      mc.pow2[i] = v;
+    }
     // Per-warp constant byte offsets, so that a tile costs only its loads, its
     // decode and its store: the lane's three window words inside a tile, and
     // where each of this warp's tiles lands in the decoded operand.

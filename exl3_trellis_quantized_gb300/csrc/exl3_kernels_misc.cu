@@ -9,6 +9,8 @@ namespace exl3 {
 // TensorFold PR #740, "Arithmetic": parts are summed in a fixed part order).  One warp per (row, 128-column block); lane l owns
 // columns 4l..4l+3 of the block: z = ((p0 + p1) + p2) + ..., then the same
 // butterfly, scale and rounding as the fused epilogue, then zeros written back.
+// P is a template argument, so a thread holds exactly P partials.
+template <int P>
 __global__ void __launch_bounds__(256) splitk_epilogue_kernel(const GemmArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t cb = a.n >> 7;
@@ -21,17 +23,22 @@ __global__ void __launch_bounds__(256) splitk_epilogue_kernel(const GemmArgs a) 
     const int64_t r = u / cb;
     const int64_t col = (u - r * cb) * 128 + 4 * lane;
     float* p = a.acc + r * a.n + col;
-    float4 s = *reinterpret_cast<const float4*>(p);
-    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int part = 1; part < a.parts; ++part) {
-      float* q = p + part * plane;
-      const float4 t = *reinterpret_cast<const float4*>(q);
-      s.x = s.x + t.x;
-      s.y = s.y + t.y;
-      s.z = s.z + t.z;
-      s.w = s.w + t.w;
-      *reinterpret_cast<float4*>(q) = make_float4(0.f, 0.f, 0.f, 0.f);
+    // every part's partial first (all loads in flight together; a zero store
+    // between them would order each load after the previous store), then the
+    // sum in part order, then the zeros
+    float4 t[P];
+#pragma unroll
+    for (int part = 0; part < P; ++part) t[part] = __ldcs(reinterpret_cast<const float4*>(p + part * plane));
+    float4 s = t[0];
+#pragma unroll
+    for (int part = 1; part < P; ++part) {
+      s.x = s.x + t[part].x;
+      s.y = s.y + t[part].y;
+      s.z = s.z + t[part].z;
+      s.w = s.w + t[part].w;
     }
+#pragma unroll
+    for (int part = 0; part < P; ++part) __stcs(reinterpret_cast<float4*>(p + part * plane), make_float4(0.f, 0.f, 0.f, 0.f));
     float v[4] = {s.x, s.y, s.z, s.w};
     fwht128_warp(v, lane);
     const uint2 sv = *reinterpret_cast<const uint2*>(a.svh + col);
@@ -53,7 +60,15 @@ cudaError_t launch_splitk_epilogue(const GemmArgs& a, cudaStream_t stream) {
   const int64_t units = a.m * (a.n >> 7);
   const int64_t want = (units + 7) / 8;
   const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
-  splitk_epilogue_kernel<<<blocks, 256, 0, stream>>>(a);
+  switch (a.parts) {  // exl3_splitk_parts returns 2..16 whenever this runs
+#define EXL3_SPLITK_CASE(P) \
+  case P: splitk_epilogue_kernel<P><<<blocks, 256, 0, stream>>>(a); break;
+    EXL3_SPLITK_CASE(2) EXL3_SPLITK_CASE(3) EXL3_SPLITK_CASE(4) EXL3_SPLITK_CASE(5) EXL3_SPLITK_CASE(6)
+    EXL3_SPLITK_CASE(7) EXL3_SPLITK_CASE(8) EXL3_SPLITK_CASE(9) EXL3_SPLITK_CASE(10) EXL3_SPLITK_CASE(11)
+    EXL3_SPLITK_CASE(12) EXL3_SPLITK_CASE(13) EXL3_SPLITK_CASE(14) EXL3_SPLITK_CASE(15) EXL3_SPLITK_CASE(16)
+#undef EXL3_SPLITK_CASE
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
