@@ -74,10 +74,10 @@ struct TcCfg {
   static constexpr int kAvail = kTcSmemBudget - 1024 - kCtrlBytes;
   // Ring depths: three decoded-operand slots when two activation slots and
   // four trellis slots still fit, else two; then four activation slots for
-  // small batches (they are small), otherwise three if four trellis slots
+  // small batches (they are small), otherwise three, if four trellis slots
   // still fit, else two; the trellis ring takes the rest.
   static constexpr int kNW = (kAvail - 2 * kXSlot - 3 * kWSlot >= 4 * kTSlot) ? 3 : 2;
-  static constexpr int kNX = XR < 128 ? 4 : (kAvail - 3 * kXSlot - kNW * kWSlot >= 4 * kTSlot) ? 3 : 2;
+  static constexpr int kNX = (kAvail - (XR < 128 ? 4 : 3) * kXSlot - kNW * kWSlot >= 4 * kTSlot) ? (XR < 128 ? 4 : 3) : 2;
   static constexpr int kNT0 = (kAvail - kNX * kXSlot - kNW * kWSlot) / kTSlot;
   static constexpr int kNT = kNT0 > 16 ? 16 : kNT0;
   static constexpr int kXRing = 0;  // byte offsets of the rings
@@ -91,7 +91,7 @@ struct TcCfg {
   static constexpr int kTpw = kTiles / kTcDecodeWarps;  // per decoder warp
   static constexpr int kZStride = BN + 4;               // epilogue staging row stride (floats)
   static_assert(RG * BN <= 512, "accumulators exceed tensor memory");
-  static_assert(kNT >= 4, "not enough shared memory for four trellis slots");
+  static_assert(kNT >= 2, "not enough shared memory for two trellis slots");
   static_assert(kTiles % kTcDecodeWarps == 0 && kTpw >= 1, "tiles per stage must split evenly over the decoders");
   static_assert(XR == 128 || RG == 1, "partial activation regions need a single row group");
   static_assert(kXSlot % 1024 == 0 && kWSlot % 1024 == 0, "operand slots must keep 1024-byte swizzle alignment");
@@ -542,6 +542,7 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN128R2: return launch_tc_variant<BITS, CB, 128, 2, 1, 128>(maps, p, stream);
     case TcShape::kN128R2P: return launch_tc_variant<BITS, CB, 128, 2, 1, 128, 2>(maps, p, stream);
     case TcShape::kN256R2P: return launch_tc_variant<BITS, CB, 256, 2, 1, 128, 2>(maps, p, stream);
+    case TcShape::kN128SmallK4: return launch_tc_variant<BITS, CB, 128, 1, 4, 32>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

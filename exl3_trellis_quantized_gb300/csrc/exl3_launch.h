@@ -64,12 +64,13 @@ struct TcMaps {
 enum class TcShape : int {
   kN32Small,   // BN=32,  RG=1, KA=4, XR=32   (m <= 32, narrow layers)
   kN64Small,   // BN=64,  RG=1, KA=2, XR=32   (m <= 32, wide layers)
-  kN128Small,  // BN=128, RG=1, KA=2, XR=32   (m <= 32, very wide layers, split-k parts)
+  kN128Small,  // BN=128, RG=1, KA=2, XR=32   (m <= 32, wide layers with odd k/128, split-k parts)
   kN128,       // BN=128, RG=1, KA=2, XR=128  (m <= 128)
   kN128R2,     // BN=128, RG=2, KA=1, XR=128  (large m)
   kN256R2,     // BN=256, RG=2, KA=1, XR=128  (large m, 256-aligned shard edges)
   kN128R2P,    // BN=128, RG=2, KA=1, XR=128, pair (large m)
   kN256R2P,    // BN=256, RG=2, KA=1, XR=128, pair (large m, 256-aligned shard edges)
+  kN128SmallK4,  // BN=128, RG=1, KA=4, XR=32  (m <= 32, wide layers, even k/128, no split-k)
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

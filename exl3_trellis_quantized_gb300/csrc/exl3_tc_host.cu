@@ -76,6 +76,7 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN128R2: return {128, 1, 128, 1};
     case TcShape::kN128R2P: return {128, 1, 128, 2};
     case TcShape::kN256R2P: return {256, 1, 128, 2};
+    case TcShape::kN128SmallK4: return {128, 4, 32, 1};
     default: return {256, 1, 128, 1};
   }
 }
@@ -128,7 +129,9 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r64 = small_batch_rate(a.n / 64, kRel64);
     // 32-column strips use 4 k atoms per stage: k must hold an even number of 128-blocks
     const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
-    if (r128 >= r64 && r128 >= r32) return TcShape::kN128Small;
+    // four k atoms per stage halve the per-stage synchronisation (k must hold
+    // an even number of 128-blocks)
+    if (r128 >= r64 && r128 >= r32) return (a.k / 128) % 2 == 0 ? TcShape::kN128SmallK4 : TcShape::kN128Small;
     return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
   }
   if (a.m <= 128) return TcShape::kN128;
@@ -162,7 +165,7 @@ TcShape choose_shape(const GemmArgs& a) {
 }  // namespace
 
 bool tc_shape_supported(int shape, const GemmArgs& a) {
-  if (shape < 0 || shape > (int)TcShape::kN256R2P) return false;
+  if (shape < 0 || shape > (int)TcShape::kN128SmallK4) return false;
   const TcShape s = (TcShape)shape;
   const ShapeDims d = dims_of(s);
   if (d.xr < 128 && a.m > d.xr) return false;  // small-batch shapes hold XR rows

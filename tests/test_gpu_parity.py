@@ -224,7 +224,7 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     # the cases reach every shape that their sizes allow
     need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     if not split and (k // 128) % 2 == 0:
-        need.add(0)
+        need |= {0, 8}
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
 
 
@@ -235,8 +235,8 @@ def test_tile_shape_rejections():
     xh = E.input_transform(x, suh)
     assert B.test_gemm_shape(2, xh, tr, 3, 1, svh, layer.shard_cols) is None  # 40 rows > 32
     assert B.test_gemm_shape(5, xh, tr, 3, 1, svh, layer.shard_cols) is None  # 384 columns: not 256-aligned
-    with pytest.raises(E.Exl3Error):
-        B.test_gemm_shape(8, xh, tr, 3, 1, svh, layer.shard_cols)
+    with pytest.raises(E.Exl3Error):  # past the last shape
+        B.test_gemm_shape(B.TEST_TILE_SHAPES, xh, tr, 3, 1, svh, layer.shard_cols)
 
 
 def test_fused_shards_equal_separate_launches():
