@@ -286,31 +286,67 @@ def run_gpu(args, wl_name):
                       "pct_roofline": round(100.0 * sol / t, 2), "bound": b})
 
     # --- end to end: pinned host x -> device -> layer -> pinned host y ------
+    # Every step copies each batch's x in and its y out.  The copies run on
+    # their own streams (one per direction, so both directions overlap each
+    # other and the compute), ordered against the compute by events; device x
+    # and y are double-buffered so a copy never touches a buffer that a kernel
+    # of the other step still uses.
     xpin = [x_host[:m].clone().pin_memory() for m in ms]
     ypin = [torch.empty((m, n), dtype=torch.bfloat16).pin_memory() for m in ms]
-    xd2 = [torch.empty((m, k), dtype=torch.bfloat16, device=dev) for m in ms]
+    xd2 = [[torch.empty((m, k), dtype=torch.bfloat16, device=dev) for m in ms] for _ in range(2)]
+    yd2 = [[torch.empty((m, n), dtype=torch.bfloat16, device=dev) for m in ms] for _ in range(2)]
     h2d = sum(t.numel() * 2 for t in xpin)
     d2h = sum(t.numel() * 2 for t in ypin)
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    x_in = [[ev() for _ in ms] for _ in range(2)]     # x copied in
+    x_free = [[ev() for _ in ms] for _ in range(2)]   # transform done with x
+    y_done = [[ev() for _ in ms] for _ in range(2)]   # y computed
+    y_free = [[ev() for _ in ms] for _ in range(2)]   # y copied out
+    used = [[False] * len(ms) for _ in range(2)]
 
     def e2e_step(it):
+        b = it % 2
         for i in range(len(ms)):
-            xd2[i].copy_(xpin[i], non_blocking=True)
+            with torch.cuda.stream(h2d_stream):
+                if used[b][i]:
+                    h2d_stream.wait_event(x_free[b][i])
+                xd2[b][i].copy_(xpin[i], non_blocking=True)
+                x_in[b][i].record(h2d_stream)
+            stream.wait_event(x_in[b][i])
+            if used[b][i]:
+                stream.wait_event(y_free[b][i])
             tr = trs[(it + i) % copies]
-            E.input_transform(xd2[i], suh, xh[i])
+            E.input_transform(xd2[b][i], suh, xh[i])
+            x_free[b][i].record(stream)
             if split:
-                E.gemm_splitk(xh[i], tr, bits, cb, svh, layer.shard_cols, accs[i], out=ys[i])
+                E.gemm_splitk(xh[i], tr, bits, cb, svh, layer.shard_cols, accs[i], out=yd2[b][i])
             else:
-                E.gemm(xh[i], tr, bits, cb, svh, layer.shard_cols, out=ys[i])
-            ypin[i].copy_(ys[i], non_blocking=True)
+                E.gemm(xh[i], tr, bits, cb, svh, layer.shard_cols, out=yd2[b][i])
+            y_done[b][i].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(y_done[b][i])
+                ypin[i].copy_(yd2[b][i], non_blocking=True)
+                y_free[b][i].record(d2h_stream)
+            used[b][i] = True
+
+    def join_copies():
+        stream.wait_stream(h2d_stream)
+        stream.wait_stream(d2h_stream)
 
     for w in range(max(1, args.warmup)):
         e2e_step(w)
+    join_copies()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    h2d_stream.wait_event(e0)
+    d2h_stream.wait_event(e0)
     for s in range(args.steps):
         e2e_step(s)
+    join_copies()
     e1.record(stream)
     torch.cuda.synchronize()
     e_el = e0.elapsed_time(e1) / 1e3

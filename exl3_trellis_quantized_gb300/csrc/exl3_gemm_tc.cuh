@@ -90,6 +90,10 @@ struct TcCfg {
   static constexpr int kTiles = kTrRows * (kBNL / 16);  // tiles decoded per stage
   static constexpr int kTpw = kTiles / kTcDecodeWarps;  // per decoder warp
   static constexpr int kZStride = BN + 4;               // epilogue staging row stride (floats)
+  // Decoders decode a stage into registers before waiting for its operand
+  // slot, except in the single-row-group, full-row shape, where that order
+  // measured slower on GB300.
+  static constexpr bool kDecodeFirst = !(RG == 1 && XR == 128);
   static_assert(RG * BN <= 512, "accumulators exceed tensor memory");
   static_assert(kNT >= 2, "not enough shared memory for two trellis slots");
   static_assert(kTiles % kTcDecodeWarps == 0 && kTpw >= 1, "tiles per stage must split evenly over the decoders");
@@ -340,15 +344,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         wv[i][1] = ld_shared_u32(trbase + word_off[1] + i * kStep);
         wv[i][2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2] + i * kStep) : 0u;
       }
-      // the decoded-operand slot must have been consumed by the MMA(s) of its last use
-      if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
       const uint32_t wbase = wring_u32 + (uint32_t)(ws * C::kWSlot);
+      if constexpr (C::kDecodeFirst) {
+        // decode into registers first, so that waiting for the decoded-operand
+        // slot (consumed by the MMA(s) of its last use) overlaps the arithmetic
+        uint32_t b[C::kTpw][4];
 #pragma unroll
-      for (int i = 0; i < C::kTpw; ++i) {
-        const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
-        uint32_t b[4];
-        decode_lane<BITS, CB>(al, mc, b);
-        stmatrix_x4(wbase + w_off[i], b[0], b[1], b[2], b[3]);
+        for (int i = 0; i < C::kTpw; ++i) {
+          const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
+          decode_lane<BITS, CB>(al, mc, b[i]);
+        }
+        if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+#pragma unroll
+        for (int i = 0; i < C::kTpw; ++i) stmatrix_x4(wbase + w_off[i], b[i][0], b[i][1], b[i][2], b[i][3]);
+      } else {
+        if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+#pragma unroll
+        for (int i = 0; i < C::kTpw; ++i) {
+          const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
+          uint32_t b[4];
+          decode_lane<BITS, CB>(al, mc, b);
+          stmatrix_x4(wbase + w_off[i], b[0], b[1], b[2], b[3]);
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
