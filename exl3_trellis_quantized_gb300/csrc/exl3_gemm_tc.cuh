@@ -207,6 +207,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---------------- activation producer ----------------
     if (lane == 0) {
       prefetch_tensormap(&maps.xh);
+      // The activations may come from the kernel just before this one in the
+      // stream (the input transform, which lets this grid start early): wait
+      // for it here.  Everything else this kernel reads before the wait (the
+      // trellis, svh) is weights, which no kernel of this library writes.
+      pdl_wait();
       const uint32_t tx = (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
       int s = 0;
       uint32_t ph = 0;
@@ -538,13 +543,17 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = C::kClusterX;
   attr[0].val.clusterDim.y = PAIR;
   attr[0].val.clusterDim.z = 1;
+  // may start while the previous kernel (the input transform) still runs;
+  // the activation producer waits for it (pdl_wait) before reading xh
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, maps, p);
 }
 

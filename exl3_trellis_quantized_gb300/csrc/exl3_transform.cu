@@ -17,6 +17,7 @@
 // element.
 #include "exl3_device.cuh"
 #include "exl3_launch.h"
+#include "exl3_sm100.cuh"
 
 namespace exl3 {
 
@@ -42,6 +43,9 @@ template <bool X_BF16>
 __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
                                                               const uint16_t* __restrict__ suh, int num_shards,
                                                               uint16_t* __restrict__ xh) {
+  // The GEMM that consumes xh may be scheduled now: it prefetches its weights
+  // and waits for this grid to complete before it reads xh.
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int q = lane & 3;  // which 32 elements of the block
   const int64_t kb = k >> 7;

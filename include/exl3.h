@@ -91,6 +91,14 @@ exl3_status_t exl3_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t 
  *   shard_cols HOST, int32 [num_shards+1]: 0 = c_0 < c_1 < ... < c_S = n, multiples
  *              of 128; shard s owns output columns [c_s, c_{s+1})
  *   y          device, [m][n] of y_dtype (output)
+ *
+ * Launch overlap: the GEMM kernel is launched with programmatic stream
+ * serialization, and exl3_input_transform's kernel lets its dependents start
+ * early.  So the GEMM may begin (and read trellis and svh) while the kernel
+ * before it in the stream is still running, provided that kernel allows it;
+ * it reads xh and writes y only after that kernel has completed.  A caller's
+ * own kernel that allows early dependents must therefore not write the
+ * trellis or svh that the following GEMM uses.
  */
 exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis,
                         int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
