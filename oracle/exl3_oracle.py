@@ -284,6 +284,28 @@ def input_transform(x, suh) -> np.ndarray:
     return np.stack([blockwise_hadamard(x * suh[s][None, :]) * 2.0 ** -4 for s in range(suh.shape[0])])
 
 
+def swiglu(gate_up) -> np.ndarray:
+    """h = silu(gate) * up, float64 [m, K] from gate_up [m, 2K].
+
+    The down-projection's input of a gated MLP, folded into its input
+    transform (cuda-exl3 README, "MoE throughput": SwiGLU folded into the
+    down-projection's input transform).  The pages print no formula; this
+    module reads it as the usual SwiGLU, silu(g) * u with silu(g) = g / (1 +
+    e^-g), gate in the first K columns and up in the last K (the column order
+    of a gate_up layer fused as two shards).
+    """
+    gu = np.asarray(gate_up, dtype=np.float64)
+    k = gu.shape[1] // 2
+    g, u = gu[:, :k], gu[:, k:]
+    with np.errstate(over="ignore"):  # e^-g overflows to inf for very negative g: silu -> -0
+        return g / (1.0 + np.exp(-g)) * u
+
+
+def input_transform_swiglu(gate_up, suh) -> np.ndarray:
+    """x' = H(swiglu(gate_up) * suh) * 2^-4 per shard, float64 [S, m, K]."""
+    return input_transform(swiglu(gate_up), suh)
+
+
 def output_transform(z, svh) -> np.ndarray:
     """y = H(z) * 2^-3 * svh (TensorFold PR, "Arithmetic" step 3)."""
     return blockwise_hadamard(z) * 2.0 ** -3 * np.asarray(svh, dtype=np.float64)

@@ -303,3 +303,41 @@ def test_column_block_selection_matches_full():
     full = o.linear(x, *args)
     part = o.linear(x, *args, col_blocks=[2, 0])
     assert np.array_equal(part, np.concatenate([full[:, 256:], full[:, :128]], axis=1))
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU folded into the down-projection's input transform
+# ---------------------------------------------------------------------------
+
+
+def test_swiglu_closed_forms():
+    g = np.array([[0.0, 1.0, -1.0, 3.0, -40.0, 40.0, -800.0]])
+    up = np.array([[2.0, 1.0, 1.0, -0.5, 1.0, 1.0, 1.0]])
+    h = o.swiglu(np.concatenate([g, up], axis=1))
+    assert h[0, 0] == 0.0  # silu(0) = 0
+    assert h[0, 1] == pytest.approx(1.0 / (1.0 + np.exp(-1.0)), rel=1e-15)  # sigmoid(1)
+    assert h[0, 2] == pytest.approx(-1.0 / (1.0 + np.e), rel=1e-15)  # -sigmoid(-1)
+    assert h[0, 3] == pytest.approx(-0.5 * 3.0 / (1.0 + np.exp(-3.0)), rel=1e-15)  # times up
+    assert abs(h[0, 4]) < 1e-15 and h[0, 5] == pytest.approx(40.0, rel=1e-15)  # tails: 0 and identity
+    assert h[0, 6] == 0.0  # e^800 overflows: the result is a signed zero, not a NaN
+
+
+def test_swiglu_identities():
+    """silu(g) - silu(-g) = g (sigmoid(g) + sigmoid(-g) = 1), and silu agrees with
+    the independent form g/2 * (1 + tanh(g/2)); a dropped factor, a sign error
+    in the exponent or swapped gate/up halves fails one of these."""
+    g = np.linspace(-12.0, 12.0, 2001)[None]
+    one = np.ones_like(g)
+    pos = o.swiglu(np.concatenate([g, one], axis=1))
+    neg = o.swiglu(np.concatenate([-g, one], axis=1))
+    assert np.allclose(pos - neg, g, rtol=0, atol=1e-12)
+    assert np.allclose(pos, g / 2 * (1 + np.tanh(g / 2)), rtol=1e-13, atol=1e-15)
+    # gate and up are not interchangeable: the gate goes through silu, up does not
+    up = np.full_like(g, 3.0)
+    assert np.allclose(o.swiglu(np.concatenate([g, up], axis=1)), 3.0 * pos, rtol=1e-15, atol=0)
+
+
+def test_swiglu_transform_is_the_transform_of_swiglu():
+    gu = synthetic.make_x(9, 512, seed=61).double().numpy()
+    suh = np.random.default_rng(62).uniform(0.5, 1.5, (2, 256))
+    assert np.array_equal(o.input_transform_swiglu(gu, suh), o.input_transform(o.swiglu(gu), suh))
