@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     gemm,
     gemm_splitk,
     input_transform,
+    input_transform_swiglu,
     lib,
     linear,
     splitk_parts,

@@ -43,6 +43,8 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(_LIB_PATH)
     vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
     L.exl3_input_transform.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
+    L.exl3_input_transform_swiglu.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
+    L.exl3_input_transform_swiglu.restype = ctypes.c_int
     L.exl3_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, ctypes.c_int, i64, vp]
     L.exl3_gemm_splitk.argtypes = L.exl3_gemm.argtypes[:-1] + [vp, sz, vp]
     L.exl3_gemm_splitk_noalloc.argtypes = L.exl3_gemm.argtypes
@@ -127,6 +129,27 @@ def input_transform(x: torch.Tensor, suh: torch.Tensor, out: Optional[torch.Tens
     st = lib().exl3_input_transform(_ptr(x), _BF16 if x.dtype == torch.bfloat16 else _F16, m, k, _ptr(suh), s,
                                     _ptr(out), _stream(x))
     _check(st, "exl3_input_transform")
+    return out
+
+
+def input_transform_swiglu(gate_up: torch.Tensor, suh: torch.Tensor,
+                           out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """xh[s] = fp16(H(silu(gate) * up * suh[s]) * 2^-4); gate_up bf16/fp16 [m, 2k] (gate first), suh fp16 [S, k]."""
+    if gate_up.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("gate_up must be bf16 or fp16")
+    _need(gate_up, gate_up.dtype, "gate_up")
+    _need(suh, torch.float16, "suh")
+    m, k2 = gate_up.shape
+    if k2 % 2:
+        raise ValueError("gate_up holds gate and up halves")
+    k = k2 // 2
+    s = suh.shape[0]
+    if out is None:
+        out = torch.empty((s, m, k), dtype=torch.float16, device=gate_up.device)
+    _need(out, torch.float16, "out")
+    st = lib().exl3_input_transform_swiglu(_ptr(gate_up), _BF16 if gate_up.dtype == torch.bfloat16 else _F16, m, k,
+                                           _ptr(suh), s, _ptr(out), _stream(gate_up))
+    _check(st, "exl3_input_transform_swiglu")
     return out
 
 

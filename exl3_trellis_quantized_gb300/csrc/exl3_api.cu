@@ -83,6 +83,18 @@ exl3_status_t exl3_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t 
                      "exl3_input_transform");
 }
 
+exl3_status_t exl3_input_transform_swiglu(const void* gate_up, exl3_dtype_t dtype, int64_t m, int64_t k,
+                                          const uint16_t* suh, int32_t num_shards, uint16_t* xh, void* stream) {
+  if (m < 0 || m > kMaxRows || !valid_kn(k) || !valid_dtype(dtype)) return EXL3_EINVAL;
+  if (num_shards < 1 || num_shards > EXL3_MAX_SHARDS) return EXL3_EINVAL;
+  if (!aligned16(suh)) return EXL3_EINVAL;
+  if (m == 0) return EXL3_OK;
+  if (!aligned16(gate_up) || !aligned16(xh)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_input_transform_swiglu(gate_up, dtype == EXL3_BF16, m, k, suh, num_shards, xh,
+                                                         static_cast<cudaStream_t>(stream)),
+                     "exl3_input_transform_swiglu");
+}
+
 exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
                         exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
                         void* y, exl3_dtype_t y_dtype, int64_t n, void* stream) {

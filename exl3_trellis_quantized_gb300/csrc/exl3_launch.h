@@ -38,6 +38,10 @@ struct GemmArgs {
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
                                    int num_shards, uint16_t* xh, cudaStream_t stream);
 
+// The same with the input computed as silu(gate) * up from gate_up [m][2k].
+cudaError_t launch_input_transform_swiglu(const void* gate_up, bool bf16, int64_t m, int64_t k, const uint16_t* suh,
+                                          int num_shards, uint16_t* xh, cudaStream_t stream);
+
 // Sum the P partials in part order, rotate, scale, store y, zero the workspace.
 cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
 

@@ -32,6 +32,46 @@ __device__ __forceinline__ void unpack8(const uint4 w, uint16_t (&e)[8]) {
   }
 }
 
+// The Hadamard butterfly of a lane's 32 values (stages of stride 1..16 in
+// registers, 32 and 64 with lanes q^1 and q^2), times 2^-4, rounded to fp16
+// and stored at dst (nothing is stored when dst is null; the lane still takes
+// part in the exchanges).
+__device__ __forceinline__ void rotate_store(float (&v)[32], int q, uint16_t* dst) {
+#pragma unroll
+  for (int st = 1; st < 32; st <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if ((i & st) == 0) {
+        const float a = v[i], b = v[i + st];
+        v[i] = a + b;
+        v[i + st] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int st = 1; st <= 2; st <<= 1) {  // element strides 32 and 64
+    const bool upper = (q & st) != 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float p = __shfl_xor_sync(0xffffffffu, v[i], st);
+      v[i] = upper ? (p - v[i]) : (v[i] + p);
+    }
+  }
+  if (dst != nullptr) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint16_t lo = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i] * 0.0625f));  // 2^-4 exact
+        const uint16_t hi = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i + 1] * 0.0625f));
+        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 }  // namespace
 
 template <bool X_BF16>
@@ -85,40 +125,7 @@ __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[8 * c + i] = to_f32<X_BF16>(e[i]) * __half2float(__ushort_as_half(se[i]));  // exact
       }
-#pragma unroll
-      for (int st = 1; st < 32; st <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          if ((i & st) == 0) {
-            const float a = v[i], b = v[i + st];
-            v[i] = a + b;
-            v[i + st] = a - b;
-          }
-        }
-      }
-#pragma unroll
-      for (int st = 1; st <= 2; st <<= 1) {  // element strides 32 and 64
-        const bool upper = (q & st) != 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p = __shfl_xor_sync(0xffffffffu, v[i], st);
-          v[i] = upper ? (p - v[i]) : (v[i] + p);
-        }
-      }
-      if (off >= 0) {
-        uint16_t* dst = xh + (int64_t)s * m * k + off;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint16_t lo = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i] * 0.0625f));  // 2^-4 exact
-            const uint16_t hi = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i + 1] * 0.0625f));
-            w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
-          }
-          *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
+      rotate_store(v, q, off >= 0 ? xh + (int64_t)s * m * k + off : nullptr);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
@@ -127,20 +134,96 @@ __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __
   }
 }
 
+// SwiGLU folded into the transform (cuda-exl3 README, "MoE throughput"): the
+// input is a gated MLP's gate_up output [m][2k]; each element of the
+// down-projection's input is h = silu(g) * u in fp32, silu(g) = g / (1 + e^-g),
+// with g from the first k columns and u from the last k, and h then takes the
+// place of x above.  Same lane layout; the next pass's words are prefetched.
+template <bool X_BF16>
+__global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint16_t* __restrict__ gu, int64_t m,
+                                                                     int64_t k, const uint16_t* __restrict__ suh,
+                                                                     int num_shards, uint16_t* __restrict__ xh) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int q = lane & 3;
+  const int64_t kb = k >> 7;
+  const int64_t units = m * kb;
+  const int64_t groups = (units + 7) / 8;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  // (row, column) of this lane's 32 values in group g; false past the end
+  auto lane_pos = [&](int64_t g, int64_t* row, int64_t* col) -> bool {
+    const int64_t u = g * 8 + (lane >> 2);
+    if (g >= groups || u >= units) return false;
+    *row = u / kb;
+    *col = (u - *row * kb) * 128 + 32 * q;
+    return true;
+  };
+  auto load = [&](bool ok, int64_t row, int64_t col, uint4 (&gw)[4], uint4 (&uw)[4]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      gw[c] = ok ? *reinterpret_cast<const uint4*>(gu + row * 2 * k + col + 8 * c) : make_uint4(0, 0, 0, 0);
+      uw[c] = ok ? *reinterpret_cast<const uint4*>(gu + row * 2 * k + k + col + 8 * c) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int64_t row = 0, col = 0;
+  bool ok = lane_pos(g, &row, &col);
+  uint4 cg[4], cu[4];
+  load(ok, row, col, cg, cu);
+  for (; g < groups; g += warps_total) {
+    int64_t nrow = 0, ncol = 0;
+    const bool nok = lane_pos(g + warps_total, &nrow, &ncol);
+    uint4 ng[4], nu[4];
+    load(nok, nrow, ncol, ng, nu);
+    float h[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint16_t ge[8], ue[8];
+      unpack8(cg[c], ge);
+      unpack8(cu[c], ue);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float gv = to_f32<X_BF16>(ge[i]);
+        h[8 * c + i] = gv / (1.0f + expf(-gv)) * to_f32<X_BF16>(ue[i]);
+      }
+    }
+    const int64_t c0 = ok ? col : 32 * q;
+    for (int s = 0; s < num_shards; ++s) {
+      float v[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint16_t se[8];
+        unpack8(*reinterpret_cast<const uint4*>(suh + (int64_t)s * k + c0 + 8 * c), se);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[8 * c + i] = h[8 * c + i] * __half2float(__ushort_as_half(se[i]));
+      }
+      rotate_store(v, q, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      cg[c] = ng[c];
+      cu[c] = nu[c];
+    }
+    ok = nok;
+    row = nrow;
+    col = ncol;
+  }
+}
+
 namespace {
 
 // Blocks that stay resident on the device at once (read once per device and
 // kernel variant): the grid is exactly that, so every warp streams through many
 // passes with the next pass's loads in flight.
-template <bool X_BF16>
-int resident_blocks(int threads) {
-  static int cache[64] = {};
+template <int ID, typename Kernel>
+int resident_blocks(Kernel kern, int threads) {
+  static int cache[64] = {};  // one cache per ID (one ID per kernel)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152 * 2;
   if (cache[dev] == 0) {
     int sms = 0, per_sm = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, input_transform_kernel<X_BF16>, threads, 0);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
     cache[dev] = (sms > 0 ? sms : 152) * (per_sm > 0 ? per_sm : 1);  // benign race: same value
   }
   return cache[dev];
@@ -153,12 +236,31 @@ cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_
   const int64_t groups = (m * (k >> 7) + 7) / 8;  // one warp pass each
   const int threads = 256;
   const int64_t want = (groups + 7) / 8;
-  const int cap = x_bf16 ? resident_blocks<true>(threads) : resident_blocks<false>(threads);
+  const int cap = x_bf16 ? resident_blocks<0>(input_transform_kernel<true>, threads)
+                         : resident_blocks<1>(input_transform_kernel<false>, threads);
   const int blocks = (int)(want < cap ? want : cap);
   if (x_bf16) {
     input_transform_kernel<true><<<blocks, threads, 0, stream>>>((const uint16_t*)x, m, k, suh, num_shards, xh);
   } else {
     input_transform_kernel<false><<<blocks, threads, 0, stream>>>((const uint16_t*)x, m, k, suh, num_shards, xh);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_input_transform_swiglu(const void* gate_up, bool bf16, int64_t m, int64_t k, const uint16_t* suh,
+                                          int num_shards, uint16_t* xh, cudaStream_t stream) {
+  const int64_t groups = (m * (k >> 7) + 7) / 8;
+  const int threads = 256;
+  const int64_t want = (groups + 7) / 8;
+  const int cap = bf16 ? resident_blocks<2>(input_transform_swiglu_kernel<true>, threads)
+                       : resident_blocks<3>(input_transform_swiglu_kernel<false>, threads);
+  const int blocks = (int)(want < cap ? want : cap);
+  if (bf16) {
+    input_transform_swiglu_kernel<true><<<blocks, threads, 0, stream>>>((const uint16_t*)gate_up, m, k, suh,
+                                                                        num_shards, xh);
+  } else {
+    input_transform_swiglu_kernel<false><<<blocks, threads, 0, stream>>>((const uint16_t*)gate_up, m, k, suh,
+                                                                         num_shards, xh);
   }
   return cudaGetLastError();
 }

@@ -71,6 +71,25 @@ exl3_status_t exl3_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t 
                                    void* stream);
 
 /*
+ * exl3_input_transform_swiglu -- the down-projection's input transform with the
+ * gated MLP's SwiGLU folded in (cuda-exl3 README, "MoE throughput": folding
+ * SwiGLU into the down-projection's input transform removes an elementwise
+ * pass).  The pages print no formula; this library reads it as the usual
+ * SwiGLU with the gate first:
+ *     h[r][j]      = silu(g) * u,  g = gate_up[r][j], u = gate_up[r][k + j],
+ *                    silu(g) = g / (1 + e^-g), in fp32
+ *     xh[s][r][:]  = as exl3_input_transform with h in place of x
+ * (the layout a gate_up layer fused as two shards of width k writes).
+ *   gate_up  device, [m][2k] of dtype (bf16 or fp16), 16-byte aligned
+ *   suh      device, fp16 [num_shards][k]
+ *   xh       device, fp16 [num_shards][m][k] (output)
+ * Validation and the empty batch as for exl3_input_transform.
+ */
+exl3_status_t exl3_input_transform_swiglu(const void* gate_up, exl3_dtype_t dtype, int64_t m, int64_t k,
+                                          const uint16_t* suh, int32_t num_shards, uint16_t* xh,
+                                          void* stream);
+
+/*
  * exl3_gemm -- trellis decode fused into the contraction, output rotation fused
  * into the epilogue, all shards of a fused layer in one launch.
  *

@@ -105,6 +105,15 @@ def test_input_transform_rejects_invalid(L):
     assert L.exl3_input_transform(v, 1, 0, 256, v, 1, v, None) == 0
 
 
+def test_swiglu_transform_rejects_invalid(L):
+    v = ctypes.c_void_p(FAKE)
+    assert L.exl3_input_transform_swiglu(v, 1, 4, 200, v, 1, v, None) == 1  # k not a multiple of 128
+    assert L.exl3_input_transform_swiglu(v, 1, 4, 256, v, 0, v, None) == 1  # no shard
+    assert L.exl3_input_transform_swiglu(v, 2, 4, 256, v, 1, v, None) == 1  # dtype
+    assert L.exl3_input_transform_swiglu(ctypes.c_void_p(FAKE + 4), 1, 4, 256, v, 1, v, None) == 1
+    assert L.exl3_input_transform_swiglu(v, 1, 0, 256, v, 1, v, None) == 0  # empty batch
+
+
 def test_test_entry_points_reject_invalid(L):
     v = ctypes.c_void_p(FAKE)
     assert L.exl3_test_codebook(7, v, None) == 1
