@@ -509,18 +509,112 @@ def run_reference(args, wl_name):
     }
 
 
+# ---------------------------------------------------------------------------
+# Gated MLP block: gate_up GEMM -> SwiGLU folded into the down-projection's
+# input transform -> split-k down GEMM (a non-default workload)
+# ---------------------------------------------------------------------------
+MLP = {"hidden": 5120, "inter": 17408, "gate_up": (5, 2), "down": (6, 2), "m": [1, 16, 128, 512]}
+
+
+def run_mlp(args):
+    import torch
+
+    import exl3_trellis_quantized_gb300 as E
+    from exl3_trellis_quantized_gb300 import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E.lib()
+    peaks, peak_src = load_peaks()
+    hid, inter, ms = MLP["hidden"], MLP["inter"], MLP["m"]
+    (gb, gcb), (db, dcb) = MLP["gate_up"], MLP["down"]
+    gu = synthetic.make_layer(hid, [inter, inter], gb, gcb, seed=1101)
+    dn = synthetic.make_layer(inter, [hid], db, dcb, seed=1102)
+    wbytes = (gu.trellis.numel() + dn.trellis.numel()) * 2
+    copies = max(3, -(-3 * L2_BYTES // wbytes))
+    gtr = [gu.trellis.to(dev)] + [None] * (copies - 1)
+    dtr = [dn.trellis.to(dev)] + [None] * (copies - 1)
+    for c in range(1, copies):
+        gtr[c], dtr[c] = gtr[0].clone(), dtr[0].clone()
+    gsuh, gsvh, dsuh, dsvh = gu.suh.to(dev), gu.svh.to(dev), dn.suh.to(dev), dn.svh.to(dev)
+    x = synthetic.make_x(max(ms), hid, seed=1103).to(dev)
+    bufs = {}
+    for m in ms:
+        bufs[m] = dict(xh=torch.empty((2, m, hid), dtype=torch.float16, device=dev),
+                       g=torch.empty((m, 2 * inter), dtype=torch.bfloat16, device=dev),
+                       h=torch.empty((m, inter), dtype=torch.bfloat16, device=dev),
+                       dxh=torch.empty((1, m, inter), dtype=torch.float16, device=dev),
+                       y=torch.empty((m, hid), dtype=torch.bfloat16, device=dev),
+                       acc=torch.zeros(max(1, E.splitk_workspace_bytes(m, inter, hid) // 4), dtype=torch.float32,
+                                       device=dev))
+
+    def block(m, it, fused):
+        b = bufs[m]
+        c = it % copies
+        E.input_transform(x[:m], gsuh, b["xh"])
+        E.gemm(b["xh"], gtr[c], gb, gcb, gsvh, gu.shard_cols, out=b["g"])
+        if fused:
+            E.input_transform_swiglu(b["g"], dsuh, b["dxh"])
+        else:  # the same step unfused: torch's silu and product, then the plain transform
+            torch.mul(torch.nn.functional.silu(b["g"][:, :inter]), b["g"][:, inter:], out=b["h"])
+            E.input_transform(b["h"], dsuh, b["dxh"])
+        E.gemm_splitk(b["dxh"], dtr[c], db, dcb, dsvh, dn.shard_cols, b["acc"], out=b["y"])
+
+    def timed(fused):
+        for w in range(args.warmup):
+            for m in ms:
+                block(m, w, fused)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s in range(args.steps):
+            for m in ms:
+                block(m, s, fused)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / args.steps
+
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    t_fused = timed(True)
+    clk = clocks.stop()
+    t_unfused = timed(False)
+    sol = sum(sol_seconds(m, hid, 2 * inter, gb, peaks)[0] + sol_seconds(m, inter, hid, db, peaks)[0] for m in ms)
+    return {
+        "metric": "EXL3 gated MLP block (gate_up, SwiGLU folded into the down transform, split-k down) %roofline",
+        "value": round(100.0 * sol / t_fused, 3), "unit": "% of 1-GPU roofline (both GEMMs' SoL / measured)",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_fused * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 products, fp32 sums, bf16 out",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"gated MLP hidden={hid} inter={inter}, gate_up {gb}-bit mul1 (2 shards), "
+                               f"down {db}-bit mul1 split-k, m={ms}",
+                   "l2": f"weights rotate over {copies} copies"},
+        "unfused_swiglu_ms_per_step": round(t_unfused * 1e3, 4),
+        "gpu_launches": (4 + (1 if E.splitk_parts(inter, hid) > 1 else 0)) * len(ms) * args.steps,
+        "clocks": clk, "peaks": {**peaks, "source": peak_src},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q_proj_sweep", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="q_proj_sweep", choices=sorted(WORKLOADS) + ["mlp_swiglu"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only-m", type=int, default=None,
                     help="restrict the sweep to one batch size (for profiling one launch shape)")
     args = ap.parse_args()
+    if args.workload == "mlp_swiglu":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the single-layer workloads"}))
+            return
+        args.warmup = max(args.warmup, 3)
+        print(json.dumps(run_mlp(args)), flush=True)
+        return
     if args.only_m is not None:
         d = list(WORKLOADS[args.workload])
         d[5] = [args.only_m]
