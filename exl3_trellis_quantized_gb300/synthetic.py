@@ -81,3 +81,88 @@ def random_words(count: int, seed: int) -> torch.Tensor:
     """Uniform int16 words (used for tile-level unpack tests)."""
     g = torch.Generator().manual_seed(seed)
     return torch.randint(-(1 << 15), 1 << 15, (count,), generator=g, dtype=torch.int32).to(torch.int16)
+
+
+# ---------------------------------------------------------------------------
+# Mixture-of-experts inputs
+# ---------------------------------------------------------------------------
+
+
+@dataclass
+class MoeLayer:
+    """Host copies of one EXL3 expert layer: E experts of the same shape."""
+
+    k: int
+    shard_cols: List[int]
+    bits: int
+    codebook: int
+    trellis: torch.Tensor  # int16 [E, K/16, N/16, 16*bits] (experts stacked)
+    suh: torch.Tensor  # fp16 [E, S, K]
+    svh: torch.Tensor  # fp16 [E, N]
+
+    @property
+    def n(self) -> int:
+        return self.shard_cols[-1]
+
+    @property
+    def num_experts(self) -> int:
+        return self.trellis.shape[0]
+
+
+def make_moe_layer(k: int, shard_widths: Sequence[int], bits: int, codebook: int, num_experts: int,
+                   seed: int) -> MoeLayer:
+    layers = [make_layer(k, shard_widths, bits, codebook, seed * 1009 + e) for e in range(num_experts)]
+    return MoeLayer(k=k, shard_cols=layers[0].shard_cols, bits=bits, codebook=codebook,
+                    trellis=torch.stack([l.trellis for l in layers]), suh=torch.stack([l.suh for l in layers]),
+                    svh=torch.stack([l.svh for l in layers]))
+
+
+@dataclass
+class Routing:
+    """Routed (token, expert) pairs in the block-aligned order a grouped GEMM
+    consumes (the layout vLLM's moe_align_block_size produces, cuda-exl3 README,
+    "What is supported" and "MoE notes"): pairs sorted by expert, each expert's
+    run padded to whole blocks of ``block`` rows.
+
+    sorted_ids[r] is the pair index token * topk + slot of padded row r, or
+    num_tokens * topk for a padding row; block_expert[b] is the expert of rows
+    [b * block, (b + 1) * block), or -1 for a block that belongs to no expert
+    (such blocks also sit between live ones, not only at the end).
+    """
+
+    num_tokens: int
+    topk: int
+    block: int
+    topk_ids: torch.Tensor  # int32 [num_tokens, topk], distinct experts per token
+    sorted_ids: torch.Tensor  # int32 [rows]
+    block_expert: torch.Tensor  # int32 [rows / block]
+
+    @property
+    def rows(self) -> int:
+        return self.sorted_ids.numel()
+
+
+def make_routing(num_tokens: int, num_experts: int, topk: int, block: int, seed: int,
+                 empty_blocks: int = 2) -> Routing:
+    """Random top-k choices (distinct experts per token), aligned to blocks,
+    with ``empty_blocks`` blocks of -1 inserted at random positions."""
+    g = torch.Generator().manual_seed(seed)
+    topk_ids = torch.stack([torch.randperm(num_experts, generator=g)[:topk] for _ in range(num_tokens)]).to(torch.int32)
+    pad = num_tokens * topk
+    ids: List[int] = []
+    blocks: List[int] = []
+    flat = topk_ids.reshape(-1).tolist()
+    for e in range(num_experts):
+        run = [i for i, x in enumerate(flat) if x == e]
+        if not run:
+            continue
+        nb = -(-len(run) // block)
+        run += [pad] * (nb * block - len(run))
+        ids += run
+        blocks += [e] * nb
+    for _ in range(empty_blocks):
+        at = int(torch.randint(0, len(blocks) + 1, (1,), generator=g))
+        blocks.insert(at, -1)
+        ids[at * block:at * block] = [pad] * block
+    return Routing(num_tokens=num_tokens, topk=topk, block=block, topk_ids=topk_ids,
+                   sorted_ids=torch.tensor(ids, dtype=torch.int32), block_expert=torch.tensor(blocks, dtype=torch.int32))

@@ -398,3 +398,54 @@ def linear_bruteforce(x, trellis, bits: int, cb: int, suh, svh, shard_cols: Sequ
                     acc += had(i, j) * z[128 * blk + j]
                 y[r, 128 * blk + i] = acc / 8.0 * svh[128 * blk + i]
     return y
+
+
+# ---------------------------------------------------------------------------
+# Mixture of experts (cuda-exl3 README, "What is supported": routed experts run
+# as a grouped GEMM over block-aligned (token, expert) pairs, the trellis offset
+# by a per-block expert id; exl3_moe_had_in gathers each routed row and rotates
+# it with its own expert's suh; "MoE notes": blocks of no expert carry -1 and
+# are skipped)
+# ---------------------------------------------------------------------------
+
+
+def _routed_token(sorted_ids, r: int, num_tokens: int, topk: int) -> int:
+    """Token of padded row r, or -1 for a padding row."""
+    i = int(sorted_ids[r])
+    return i // topk if 0 <= i < num_tokens * topk else -1
+
+
+def moe_input_transform(x, sorted_ids, block_expert, block: int, topk: int, suh) -> np.ndarray:
+    """xh[s, r] = the input transform of row r's token with its block's expert's
+    suh (float64 [S, rows, K]); padding rows and rows of -1 blocks are zero."""
+    x = np.asarray(x, dtype=np.float64)
+    suh = np.asarray(suh, dtype=np.float64)  # [E, S, K]
+    rows = len(sorted_ids)
+    xh = np.zeros((suh.shape[1], rows, x.shape[1]))
+    for b, e in enumerate(np.asarray(block_expert)):
+        if e < 0:
+            continue
+        for r in range(b * block, (b + 1) * block):
+            t = _routed_token(sorted_ids, r, x.shape[0], topk)
+            if t >= 0:
+                xh[:, r] = input_transform(x[t][None], suh[e])[:, 0]
+    return xh
+
+
+def moe_linear(x, sorted_ids, block_expert, block: int, topk: int, trellis, bits: int, cb: int, suh, svh,
+               shard_cols: Sequence[int]) -> np.ndarray:
+    """Rows of the grouped GEMM, float64 [rows, N]: row r is its token's output
+    through its block's expert (the layer with that expert's trellis, suh and
+    svh); padding rows are 0 and rows of -1 blocks NaN (never written)."""
+    x = np.asarray(x, dtype=np.float64)
+    rows = len(sorted_ids)
+    n = shard_cols[-1]
+    y = np.full((rows, n), np.nan)
+    for b, e in enumerate(np.asarray(block_expert)):
+        if e < 0:
+            continue
+        toks = [_routed_token(sorted_ids, r, x.shape[0], topk) for r in range(b * block, (b + 1) * block)]
+        xb = np.stack([x[t] if t >= 0 else np.zeros(x.shape[1]) for t in toks])
+        y[b * block:(b + 1) * block] = linear(xb, np.asarray(trellis[e]), bits, cb, np.asarray(suh[e]),
+                                              np.asarray(svh[e]), shard_cols)
+    return y

@@ -341,3 +341,64 @@ def test_swiglu_transform_is_the_transform_of_swiglu():
     gu = synthetic.make_x(9, 512, seed=61).double().numpy()
     suh = np.random.default_rng(62).uniform(0.5, 1.5, (2, 256))
     assert np.array_equal(o.input_transform_swiglu(gu, suh), o.input_transform(o.swiglu(gu), suh))
+
+
+# ---------------------------------------------------------------------------
+# Mixture of experts: grouped rows through each block's expert
+# ---------------------------------------------------------------------------
+
+
+def _moe_case(seed=71, tokens=7, experts=5, topk=2, block=4):
+    layer = synthetic.make_moe_layer(256, [128, 128], 3, 1, experts, seed=seed)
+    routing = synthetic.make_routing(tokens, experts, topk, block, seed=seed + 1)
+    x = synthetic.make_x(tokens, 256, seed=seed + 2).double().numpy()
+    return layer, routing, x
+
+
+def test_routing_holds_every_pair_once():
+    _, r, _ = _moe_case()
+    ids = r.sorted_ids.numpy()
+    live = ids[ids < r.num_tokens * r.topk]
+    assert sorted(live.tolist()) == list(range(r.num_tokens * r.topk))
+    assert r.rows % r.block == 0 and len(r.block_expert) == r.rows // r.block
+    assert (r.block_expert.numpy() == -1).sum() == 2
+
+
+def test_moe_rows_follow_topk_choices():
+    """Row of pair (t, j) equals the dense layer of expert topk_ids[t, j] on token
+    t, found through the routing's own top-k table rather than the block ids."""
+    layer, r, x = _moe_case()
+    y = o.moe_linear(x, r.sorted_ids.numpy(), r.block_expert.numpy(), r.block, r.topk, layer.trellis.numpy(),
+                     layer.bits, layer.codebook, layer.suh.double().numpy(), layer.svh.double().numpy(),
+                     layer.shard_cols)
+    ids = r.sorted_ids.numpy()
+    for row, pair in enumerate(ids):
+        if pair >= r.num_tokens * r.topk:
+            continue
+        t, j = divmod(int(pair), r.topk)
+        e = int(r.topk_ids[t, j])
+        want = o.linear(x[t][None], layer.trellis[e].numpy(), layer.bits, layer.codebook,
+                        layer.suh[e].double().numpy(), layer.svh[e].double().numpy(), layer.shard_cols)[0]
+        assert np.allclose(y[row], want, rtol=0, atol=1e-12)
+    blocks = r.block_expert.numpy()
+    for b, e in enumerate(blocks):
+        rows = y[b * r.block:(b + 1) * r.block]
+        if e < 0:
+            assert np.isnan(rows).all()  # skipped: never written
+        else:
+            pad = ids[b * r.block:(b + 1) * r.block] >= r.num_tokens * r.topk
+            assert (rows[pad] == 0).all()
+
+
+def test_moe_input_transform_follows_topk_choices():
+    layer, r, x = _moe_case()
+    xh = o.moe_input_transform(x, r.sorted_ids.numpy(), r.block_expert.numpy(), r.block, r.topk,
+                               layer.suh.double().numpy())
+    ids = r.sorted_ids.numpy()
+    for row, pair in enumerate(ids):
+        if pair >= r.num_tokens * r.topk:
+            assert (xh[:, row] == 0).all()
+            continue
+        t, j = divmod(int(pair), r.topk)
+        e = int(r.topk_ids[t, j])
+        assert np.array_equal(xh[:, row], o.input_transform(x[t][None], layer.suh[e].double().numpy())[:, 0])
