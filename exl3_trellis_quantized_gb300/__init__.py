@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     input_transform_swiglu,
     lib,
     linear,
+    moe_gemm,
+    moe_input_transform,
     splitk_parts,
     splitk_workspace_bytes,
     status_string,

@@ -43,6 +43,11 @@ def lib() -> ctypes.CDLL:
     L = ctypes.CDLL(_LIB_PATH)
     vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
     L.exl3_input_transform.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
+    L.exl3_moe_input_transform.argtypes = [vp, ctypes.c_int, i64, i64, vp, i64, i32, vp, i32, vp, i32, i32, vp, vp]
+    L.exl3_moe_input_transform.restype = ctypes.c_int
+    L.exl3_moe_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, i32, i32, vp, ctypes.c_int,
+                                i64, vp]
+    L.exl3_moe_gemm.restype = ctypes.c_int
     L.exl3_input_transform_swiglu.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
     L.exl3_input_transform_swiglu.restype = ctypes.c_int
     L.exl3_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, ctypes.c_int, i64, vp]
@@ -150,6 +155,51 @@ def input_transform_swiglu(gate_up: torch.Tensor, suh: torch.Tensor,
     st = lib().exl3_input_transform_swiglu(_ptr(gate_up), _BF16 if gate_up.dtype == torch.bfloat16 else _F16, m, k,
                                            _ptr(suh), s, _ptr(out), _stream(gate_up))
     _check(st, "exl3_input_transform_swiglu")
+    return out
+
+
+def moe_input_transform(x: torch.Tensor, sorted_ids: torch.Tensor, topk: int, block_expert: torch.Tensor,
+                        block: int, suh: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Gather and rotate block-aligned routed rows; suh fp16 [E, S, k] -> xh fp16 [S, rows, k]."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("x must be bf16 or fp16")
+    _need(x, x.dtype, "x")
+    _need(sorted_ids, torch.int32, "sorted_ids")
+    _need(block_expert, torch.int32, "block_expert")
+    _need(suh, torch.float16, "suh")
+    num_tokens, k = x.shape
+    e, s, _ = suh.shape
+    rows = sorted_ids.numel()
+    if out is None:
+        out = torch.empty((s, rows, k), dtype=torch.float16, device=x.device)
+    _need(out, torch.float16, "out")
+    st = lib().exl3_moe_input_transform(_ptr(x), _BF16 if x.dtype == torch.bfloat16 else _F16, num_tokens, k,
+                                        _ptr(sorted_ids), rows, int(topk), _ptr(block_expert), int(block), _ptr(suh),
+                                        s, e, _ptr(out), _stream(x))
+    _check(st, "exl3_moe_input_transform")
+    return out
+
+
+def moe_gemm(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor, shard_cols: Sequence[int],
+             block_expert: torch.Tensor, block: int, out_dtype=torch.bfloat16,
+             out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Grouped GEMM; trellis int16 [E, k/16, n/16, 16*bits], svh fp16 [E, n] -> y [rows, n] (padded-row order)."""
+    _need(xh, torch.float16, "xh")
+    _need(trellis, torch.int16, "trellis")
+    _need(svh, torch.float16, "svh")
+    _need(block_expert, torch.int32, "block_expert")
+    s, rows, k = xh.shape
+    e, n = svh.shape
+    if out is None:
+        out = torch.empty((rows, n), dtype=out_dtype, device=xh.device)
+    if out.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("output must be bf16 or fp16")
+    _need(out, out.dtype, "out")
+    cols, ns = _cols(shard_cols)
+    cbid = CODEBOOKS[cb] if isinstance(cb, str) else int(cb)
+    st = lib().exl3_moe_gemm(_ptr(xh), rows, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(block_expert),
+                             int(block), e, _ptr(out), _BF16 if out.dtype == torch.bfloat16 else _F16, n, _stream(xh))
+    _check(st, "exl3_moe_gemm")
     return out
 
 

@@ -95,6 +95,42 @@ exl3_status_t exl3_input_transform_swiglu(const void* gate_up, exl3_dtype_t dtyp
                      "exl3_input_transform_swiglu");
 }
 
+exl3_status_t exl3_moe_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t num_tokens, int64_t k,
+                                       const int32_t* sorted_ids, int64_t rows, int32_t topk,
+                                       const int32_t* block_expert, int32_t block, const uint16_t* suh,
+                                       int32_t num_shards, int32_t num_experts, uint16_t* xh, void* stream) {
+  if (num_tokens < 0 || num_tokens > kMaxRows || rows < 0 || rows > kMaxRows || !valid_kn(k)) return EXL3_EINVAL;
+  if (!valid_dtype(x_dtype) || topk < 1 || topk > 64 || (block != 32 && block != 128) || rows % block) {
+    return EXL3_EINVAL;
+  }
+  if (num_shards < 1 || num_shards > EXL3_MAX_SHARDS || num_experts < 1) return EXL3_EINVAL;
+  if (!aligned16(suh)) return EXL3_EINVAL;
+  if (rows == 0) return EXL3_OK;
+  if (!aligned16(xh) || sorted_ids == nullptr || block_expert == nullptr) return EXL3_EINVAL;
+  if (num_tokens > 0 && !aligned16(x)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_moe_input_transform(x, x_dtype == EXL3_BF16, num_tokens, k, sorted_ids, rows, topk,
+                                                      block_expert, block, suh, num_shards, num_experts, xh,
+                                                      static_cast<cudaStream_t>(stream)),
+                     "exl3_moe_input_transform");
+}
+
+exl3_status_t exl3_moe_gemm(const uint16_t* xh, int64_t rows, int64_t k, const int16_t* trellis, int32_t bits,
+                            exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
+                            const int32_t* block_expert, int32_t block, int32_t num_experts, void* y,
+                            exl3_dtype_t y_dtype, int64_t n, void* stream) {
+  exl3::GemmArgs a;
+  exl3_status_t st = check_gemm(xh, rows, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
+  if (st != EXL3_OK) return st;
+  if ((block != 32 && block != 128) || rows % block || num_experts < 1) return EXL3_EINVAL;
+  // the expert index times one expert's trellis bytes must fit the tensor map's strides
+  if ((int64_t)num_experts * (k / 16) * (n / 16) * 32 * bits > (int64_t(1) << 40)) return EXL3_EINVAL;
+  if (rows == 0) return EXL3_OK;
+  if (block_expert == nullptr) return EXL3_EINVAL;
+  a.block_expert = block_expert;
+  a.num_experts = num_experts;
+  return cuda_status(exl3::launch_moe_gemm_tc(a, bits, cb, block, static_cast<cudaStream_t>(stream)), "exl3_moe_gemm");
+}
+
 exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
                         exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
                         void* y, exl3_dtype_t y_dtype, int64_t n, void* stream) {

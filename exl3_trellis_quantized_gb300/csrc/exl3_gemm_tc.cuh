@@ -107,7 +107,10 @@ struct TcCfg {
   static_assert((2 * kNT + 2 * kNX + 3 * kNW + 1) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR>
+// MOE: grouped GEMM over row blocks of XR rows (one row group), each with its
+// own expert: blockIdx.y is the block, a.block_expert[block] the expert (the
+// trellis map then has the experts as a fourth dimension and svh is [E][n]).
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool MOE = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
@@ -117,6 +120,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int CLX = C::kClusterX;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
   const GemmArgs& a = p.a;
+  static_assert(!MOE || (RG == 1 && PAIR == 1 && BN == 128), "grouped GEMM: one row group of one CTA per block");
+  // grouped GEMM: a block of no expert (-1, or an id past the last expert) is
+  // skipped; the whole CTA leaves before it touches anything
+  int expert = 0;
+  if constexpr (MOE) {
+    expert = a.block_expert[blockIdx.y];
+    if (expert < 0 || expert >= a.num_experts) return;
+  }
+  const uint16_t* const svh = MOE ? a.svh + (int64_t)expert * a.n : a.svh;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so that
@@ -138,7 +150,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t c0 = (int64_t)blockIdx.x * BN;
-  const int64_t row0 = (int64_t)blockIdx.y * (128 * RG);
+  const int64_t row0 = (int64_t)blockIdx.y * (MOE ? XR : 128 * RG);
   const int part = (int)blockIdx.z;
   // rank within the pair (cluster dims {1, 2, 1})
   const uint32_t prank = PAIR > 1 ? cluster_ctarank() : 0u;
@@ -196,7 +208,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(&tempty[s], ph ^ 1u)) break;
         mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);  // first 64-wide k atom of the stage
-        tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, &tfull[s]);
+        if constexpr (MOE) {
+          tma_tile4d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, expert, &tfull[s]);
+        } else {
+          tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, &tfull[s]);
+        }
         if (++s == NT) {
           s = 0;
           ph ^= 1u;
@@ -415,6 +431,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
   }
   const bool bf16 = a.y_bf16 != 0;
+  // rows this CTA stores: a grouped block owns exactly its XR rows (the rows
+  // after it belong to other blocks); otherwise everything below m
+  const int64_t row_end = MOE ? row0 + XR : a.m;
   uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
   float* zs = reinterpret_cast<float*>(rings);
   constexpr int kZ = C::kZStride;
@@ -430,7 +449,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
           tmem_ld_wait();
           const int64_t row = row0 + r * 128 + quarter * 32 + lane;
-          if (ok && row < a.m) {
+          if (ok && row < row_end) {
             float4* o = reinterpret_cast<float4*>(dst + row * a.n + c0 + cc * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -451,7 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // chunk), so only the stride-32 and stride-64 stages remain.
       if (warp >= kTcFirstDecoder) {
         const int quarter = warp & 3;
-        const bool live = row0 + r * 128 + quarter * 32 < a.m;  // this quarter holds stored rows
+        const bool live = row0 + r * 128 + quarter * 32 < row_end;  // this quarter holds stored rows
         for (int cc = dw >> 2; live && cc < BN / 32; cc += kTcDecodeWarps / 4) {
           uint32_t q[32];
           tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
@@ -484,12 +503,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t src_rank = (uint32_t)(span_col / BN);
             const int local_col = span_col - (int)src_rank * BN;
             col[i] = cbase + span_col;
-            svf[i] = __half2float(__ushort_as_half(a.svh[col[i]]));
+            svf[i] = __half2float(__ushort_as_half(svh[col[i]]));
             zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
           }
           for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
             const int64_t row = row0 + r * 128 + rr;
-            if (!ok || row >= a.m) break;  // rows ascend with rr
+            if (!ok || row >= row_end) break;  // rows ascend with rr
             float v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -526,10 +545,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool MOE = false>
 cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
   using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
-  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR>;
+  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, MOE>;
   static bool configured = false;  // benign race: every thread sets the same attribute
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
@@ -538,7 +557,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
   }
   cudaLaunchConfig_t cfg = {};
   // a pair's second CTA may own only rows past m: it still decodes its half
-  const int64_t row_blocks = (p.a.m + 128 * RG - 1) / (128 * RG);
+  const int64_t row_blocks = MOE ? p.a.m / XR : (p.a.m + 128 * RG - 1) / (128 * RG);
   cfg.gridDim = dim3((unsigned)(p.a.n / BN), (unsigned)((row_blocks + PAIR - 1) / PAIR * PAIR), (unsigned)p.a.parts);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
@@ -580,6 +599,23 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
     case CB_3INST: return launch_tc_cb<BITS, CB_3INST>(maps, p, shape, stream);
     case CB_MCG: return launch_tc_cb<BITS, CB_MCG>(maps, p, shape, stream);
     default: return launch_tc_cb<BITS, CB_MUL1>(maps, p, shape, stream);
+  }
+}
+
+// Grouped GEMM: 32-row blocks on the small-batch tile, 128-row blocks on the
+// 128-row tile (both 128 columns, two k atoms per stage).
+template <int BITS, int CB>
+cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int block, cudaStream_t stream) {
+  if (block == 32) return launch_tc_variant<BITS, CB, 128, 1, 2, 32, 1, true>(maps, p, stream);
+  return launch_tc_variant<BITS, CB, 128, 1, 2, 128, 1, true>(maps, p, stream);
+}
+
+template <int BITS>
+cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int block, cudaStream_t stream) {
+  switch (cb) {
+    case CB_3INST: return launch_moe_cb<BITS, CB_3INST>(maps, p, block, stream);
+    case CB_MCG: return launch_moe_cb<BITS, CB_MCG>(maps, p, block, stream);
+    default: return launch_moe_cb<BITS, CB_MUL1>(maps, p, block, stream);
   }
 }
 

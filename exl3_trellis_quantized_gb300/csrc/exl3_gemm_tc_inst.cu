@@ -9,6 +9,8 @@
 namespace exl3 {
 template cudaError_t launch_gemm_tc_bits<EXL3_INST_BITS>(const TcMaps&, const TcParams&, int, TcShape,
                                                          cudaStream_t);
+template cudaError_t launch_moe_gemm_tc_bits<EXL3_INST_BITS>(const TcMaps&, const TcParams&, int, int,
+                                                             cudaStream_t);
 
 // This translation unit's wait-timeout flag (see exl3_sm100.cuh).
 template <>

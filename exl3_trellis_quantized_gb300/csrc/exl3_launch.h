@@ -33,6 +33,9 @@ struct GemmArgs {
   int32_t parts;  // P (1 = no split)
   int32_t y_bf16;
   DecodeConsts dc;
+  // grouped (mixture-of-experts) GEMM only: expert of each row block, or -1
+  const int32_t* block_expert;
+  int32_t num_experts;
 };
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
@@ -41,6 +44,15 @@ cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_
 // The same with the input computed as silu(gate) * up from gate_up [m][2k].
 cudaError_t launch_input_transform_swiglu(const void* gate_up, bool bf16, int64_t m, int64_t k, const uint16_t* suh,
                                           int num_shards, uint16_t* xh, cudaStream_t stream);
+
+// Gather each block-aligned routed row of x and rotate it with its block's
+// expert's suh (rows of -1 blocks untouched, padding rows zero).
+cudaError_t launch_moe_input_transform(const void* x, bool x_bf16, int64_t num_tokens, int64_t k,
+                                       const int32_t* sorted_ids, int64_t rows, int32_t topk,
+                                       const int32_t* block_expert, int32_t block, const uint16_t* suh,
+                                       int num_shards, int num_experts, uint16_t* xh, cudaStream_t stream);
+// Grouped GEMM over row blocks of `block` rows (32 or 128), one expert per block.
+cudaError_t launch_moe_gemm_tc(const GemmArgs& args, int bits, int cb, int block, cudaStream_t stream);
 
 // Sum the P partials in part order, rotate, scale, store y, zero the workspace.
 cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
@@ -86,6 +98,8 @@ bool tc_shape_supported(int shape, const GemmArgs& args);
 template <int BITS>
 cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, TcShape shape,
                                 cudaStream_t stream);
+template <int BITS>
+cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int block, cudaStream_t stream);
 // Read and clear the wait-timeout flags of every kernel translation unit (synchronous).
 cudaError_t take_device_errors(uint32_t* flags);
 template <int BITS>

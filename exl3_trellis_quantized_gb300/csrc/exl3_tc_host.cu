@@ -63,6 +63,23 @@ cudaError_t make_trellis_map(CUtensorMap* map, const int16_t* trellis, int64_t k
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Experts' trellises stacked as [E][k/16][n/16][16*bits], viewed as 4-D
+// {16*bits, n/16, k/16, E}: a copy takes one expert's tiles of a stage.
+cudaError_t make_moe_trellis_map(CUtensorMap* map, const int16_t* trellis, int64_t k, int64_t n, int bits, int bn,
+                                 int rows, int experts) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  cuuint64_t dims[4] = {(cuuint64_t)(16 * bits), (cuuint64_t)(n / 16), (cuuint64_t)(k / 16), (cuuint64_t)experts};
+  cuuint64_t strides[3] = {(cuuint64_t)(32 * bits), (cuuint64_t)((n / 16) * 32 * bits),
+                           (cuuint64_t)((k / 16) * (n / 16) * 32 * bits)};
+  cuuint32_t box[4] = {(cuuint32_t)(16 * bits), (cuuint32_t)(bn / 16), (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<int16_t*>(trellis), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 struct ShapeDims {
   int bn, ka, xr, pair;
 };
@@ -200,6 +217,27 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
     case 6: return launch_gemm_tc_bits<6>(maps, p, cb, shape, stream);
     case 7: return launch_gemm_tc_bits<7>(maps, p, cb, shape, stream);
     default: return launch_gemm_tc_bits<8>(maps, p, cb, shape, stream);
+  }
+}
+
+cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, cudaStream_t stream) {
+  TcParams p;
+  p.a = a;
+  p.box_rows = block;  // both grouped tiles take two k atoms per stage: every row of the block
+  TcMaps maps;
+  cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, 2);
+  if (e != cudaSuccess) return e;
+  e = make_moe_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, 128, 8, a.num_experts);
+  if (e != cudaSuccess) return e;
+  switch (bits) {
+    case 1: return launch_moe_gemm_tc_bits<1>(maps, p, cb, block, stream);
+    case 2: return launch_moe_gemm_tc_bits<2>(maps, p, cb, block, stream);
+    case 3: return launch_moe_gemm_tc_bits<3>(maps, p, cb, block, stream);
+    case 4: return launch_moe_gemm_tc_bits<4>(maps, p, cb, block, stream);
+    case 5: return launch_moe_gemm_tc_bits<5>(maps, p, cb, block, stream);
+    case 6: return launch_moe_gemm_tc_bits<6>(maps, p, cb, block, stream);
+    case 7: return launch_moe_gemm_tc_bits<7>(maps, p, cb, block, stream);
+    default: return launch_moe_gemm_tc_bits<8>(maps, p, cb, block, stream);
   }
 }
 

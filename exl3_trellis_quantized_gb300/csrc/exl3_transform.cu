@@ -210,6 +210,57 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
   }
 }
 
+// Mixture-of-experts gather (cuda-exl3 README, "What is supported": suh is per
+// expert, so the rotation happens after routing; each routed row is gathered and
+// rotated with its own expert's scales in one pass).  Padded row r of the
+// block-aligned routing belongs to block r / block of expert block_expert[..]
+// and to pair sorted_ids[r] = token * topk + slot (or a padding id).  Rows of a
+// block with no expert (-1, or an id past the last) are not written; padding
+// rows of live blocks get zeros.  Same lane layout as the plain transform.
+template <bool X_BF16>
+__global__ void __launch_bounds__(256) moe_input_transform_kernel(
+    const uint16_t* __restrict__ x, int64_t num_tokens, int64_t k, const int32_t* __restrict__ sorted_ids,
+    int64_t rows, int32_t topk, const int32_t* __restrict__ block_expert, int32_t block,
+    const uint16_t* __restrict__ suh, int num_shards, int num_experts, uint16_t* __restrict__ xh) {
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int q = lane & 3;
+  const int64_t kb = k >> 7;
+  const int64_t units = rows * kb;
+  const int64_t groups = (units + 7) / 8;
+  const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t pairs = num_tokens * topk;
+  for (int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < groups; g += warps_total) {
+    const int64_t u = g * 8 + (lane >> 2);
+    const bool in_range = u < units;
+    const int64_t r = in_range ? u / kb : 0;
+    const int64_t col = (in_range ? (u - r * kb) * 128 : 0) + 32 * q;
+    const int e = in_range ? block_expert[r / block] : -1;
+    const bool live = e >= 0 && e < num_experts;
+    const int64_t id = live ? (int64_t)sorted_ids[r] : -1;
+    const int64_t tok = (id >= 0 && id < pairs) ? id / topk : -1;
+    uint4 xw[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      xw[c] = tok >= 0 ? *reinterpret_cast<const uint4*>(x + tok * k + col + 8 * c) : make_uint4(0, 0, 0, 0);
+    for (int s = 0; s < num_shards; ++s) {
+      float v[32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint16_t xe[8], se[8];
+        unpack8(xw[c], xe);
+        unpack8(tok >= 0 ? *reinterpret_cast<const uint4*>(suh + ((int64_t)e * num_shards + s) * k + col + 8 * c)
+                         : make_uint4(0, 0, 0, 0),
+                se);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[8 * c + i] = to_f32<X_BF16>(xe[i]) * __half2float(__ushort_as_half(se[i]));  // exact; 0 on padding
+      }
+      rotate_store(v, q, live ? xh + ((int64_t)s * rows + r) * k + col : nullptr);
+    }
+  }
+}
+
 namespace {
 
 // Blocks that stay resident on the device at once (read once per device and
@@ -261,6 +312,28 @@ cudaError_t launch_input_transform_swiglu(const void* gate_up, bool bf16, int64_
   } else {
     input_transform_swiglu_kernel<false><<<blocks, threads, 0, stream>>>((const uint16_t*)gate_up, m, k, suh,
                                                                          num_shards, xh);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_moe_input_transform(const void* x, bool x_bf16, int64_t num_tokens, int64_t k,
+                                       const int32_t* sorted_ids, int64_t rows, int32_t topk,
+                                       const int32_t* block_expert, int32_t block, const uint16_t* suh,
+                                       int num_shards, int num_experts, uint16_t* xh, cudaStream_t stream) {
+  const int64_t groups = (rows * (k >> 7) + 7) / 8;
+  const int threads = 256;
+  const int64_t want = (groups + 7) / 8;
+  const int cap = x_bf16 ? resident_blocks<4>(moe_input_transform_kernel<true>, threads)
+                         : resident_blocks<5>(moe_input_transform_kernel<false>, threads);
+  const int blocks = (int)(want < cap ? want : cap);
+  if (x_bf16) {
+    moe_input_transform_kernel<true><<<blocks, threads, 0, stream>>>((const uint16_t*)x, num_tokens, k, sorted_ids,
+                                                                     rows, topk, block_expert, block, suh, num_shards,
+                                                                     num_experts, xh);
+  } else {
+    moe_input_transform_kernel<false><<<blocks, threads, 0, stream>>>((const uint16_t*)x, num_tokens, k, sorted_ids,
+                                                                      rows, topk, block_expert, block, suh,
+                                                                      num_shards, num_experts, xh);
   }
   return cudaGetLastError();
 }

@@ -152,6 +152,51 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
                                void* stream);
 
 /*
+ * Mixture of experts (cuda-exl3 README, "What is supported" and "MoE notes").
+ * Routed (token, expert) pairs arrive block-aligned, the layout vLLM's
+ * moe_align_block_size writes: pairs sorted by expert, each expert's run padded
+ * to whole blocks of `block` rows, so every block belongs to one expert.
+ *   sorted_ids    device int32 [rows]: pair index token * topk + slot of each
+ *                 padded row; any value outside [0, num_tokens * topk) marks
+ *                 a padding row
+ *   block_expert  device int32 [rows / block]: expert of each block; -1 (or an
+ *                 id >= num_experts) marks a block of no expert, which both
+ *                 calls skip (such blocks may sit between live ones)
+ *   block         32 or 128; rows a multiple of block
+ *
+ * exl3_moe_input_transform: since suh is per expert (and per shard), the input
+ * rotation happens after routing: each padded row of a live block gets its
+ * token's x rotated with its block's expert's suh, as exl3_input_transform
+ * computes it; padding rows get zeros; rows of skipped blocks are not written.
+ *   x    device, [num_tokens][k] of x_dtype
+ *   suh  device, fp16 [num_experts][num_shards][k]
+ *   xh   device, fp16 [num_shards][rows][k] (output)
+ *
+ * exl3_moe_gemm: the grouped GEMM.  Each live block's rows go through its
+ * expert's layer exactly as exl3_gemm computes it (same fixed fp32 order, so a
+ * row's bytes equal exl3_gemm's with that expert); skipped blocks' rows of y
+ * are not written.
+ *   xh       device, fp16 [num_shards][rows][k] (exl3_moe_input_transform's output)
+ *   trellis  device, int16 [num_experts][k/16][n/16][16*bits] (experts stacked)
+ *   svh      device, fp16 [num_experts][n]
+ *   y        device, [rows][n] of y_dtype (output, in padded-row order; the
+ *            weighted combine over each token's top-k rows is the caller's)
+ * Validation and empty input as for exl3_gemm; EXL3_EINVAL also for a block
+ * size other than 32 or 128, rows not a multiple of it, or no experts.  The
+ * kernel reads block_expert before it waits for the previous kernel in the
+ * stream, like the trellis (see exl3_gemm).
+ */
+exl3_status_t exl3_moe_input_transform(const void* x, exl3_dtype_t x_dtype, int64_t num_tokens, int64_t k,
+                                       const int32_t* sorted_ids, int64_t rows, int32_t topk,
+                                       const int32_t* block_expert, int32_t block, const uint16_t* suh,
+                                       int32_t num_shards, int32_t num_experts, uint16_t* xh, void* stream);
+exl3_status_t exl3_moe_gemm(const uint16_t* xh, int64_t rows, int64_t k, const int16_t* trellis,
+                            int32_t bits, exl3_codebook_t cb, const uint16_t* svh,
+                            const int32_t* shard_cols, int32_t num_shards, const int32_t* block_expert,
+                            int32_t block, int32_t num_experts, void* y, exl3_dtype_t y_dtype, int64_t n,
+                            void* stream);
+
+/*
  * exl3_gemm_splitk_noalloc -- the split-k GEMM for callers that cannot allocate.
  *
  * The pages have no counterpart to this call; it exists for callers that have

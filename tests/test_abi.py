@@ -114,6 +114,20 @@ def test_swiglu_transform_rejects_invalid(L):
     assert L.exl3_input_transform_swiglu(v, 1, 0, 256, v, 1, v, None) == 0  # empty batch
 
 
+def test_moe_entry_points_reject_invalid(L):
+    v = ctypes.c_void_p(FAKE)
+    cols = (ctypes.c_int32 * 2)(0, 256)
+    # block 64 / rows not a multiple of the block / no experts
+    assert L.exl3_moe_input_transform(v, 1, 4, 256, v, 64, 2, v, 64, v, 1, 4, v, None) == 1
+    assert L.exl3_moe_input_transform(v, 1, 4, 256, v, 40, 2, v, 32, v, 1, 4, v, None) == 1
+    assert L.exl3_moe_input_transform(v, 1, 4, 256, v, 64, 2, v, 32, v, 1, 0, v, None) == 1
+    assert L.exl3_moe_input_transform(v, 1, 4, 256, v, 0, 2, v, 32, v, 1, 4, v, None) == 0  # nothing routed
+    assert L.exl3_moe_gemm(v, 64, 256, v, 4, 1, v, cols, 1, v, 64, 4, v, 1, 256, None) == 1
+    assert L.exl3_moe_gemm(v, 40, 256, v, 4, 1, v, cols, 1, v, 32, 4, v, 1, 256, None) == 1
+    assert L.exl3_moe_gemm(v, 64, 256, v, 4, 1, v, cols, 1, None, 32, 4, v, 1, 256, None) == 1  # no block ids
+    assert L.exl3_moe_gemm(v, 0, 256, v, 4, 1, v, cols, 1, v, 32, 4, v, 1, 256, None) == 0
+
+
 def test_test_entry_points_reject_invalid(L):
     v = ctypes.c_void_p(FAKE)
     assert L.exl3_test_codebook(7, v, None) == 1
