@@ -596,18 +596,116 @@ def run_mlp(args):
     }
 
 
+# ---------------------------------------------------------------------------
+# Mixture of experts: gathered per-expert transform + grouped GEMM (non-default)
+# ---------------------------------------------------------------------------
+MOE = {"hidden": 2048, "inter": 768, "experts": 128, "topk": 8, "bits": 4, "cb": 1, "tokens": [1, 16, 64, 256, 1024]}
+
+
+def run_moe(args):
+    import torch
+
+    import exl3_trellis_quantized_gb300 as E
+    from exl3_trellis_quantized_gb300 import synthetic
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    E.lib()
+    peaks, peak_src = load_peaks()
+    hid, inter, ne, topk, bits, cb = (MOE[k] for k in ("hidden", "inter", "experts", "topk", "bits", "cb"))
+    n = 2 * inter  # the experts' gate_up layer, two shards
+    layer = synthetic.make_moe_layer(hid, [inter, inter], bits, cb, ne, seed=1201)
+    expert_bytes = hid * n * bits // 8
+    copies = max(3, -(-3 * L2_BYTES // (layer.trellis.numel() * 2)))
+    trs = [layer.trellis.to(dev)] + [None] * (copies - 1)
+    for c in range(1, copies):
+        trs[c] = trs[0].clone()
+    suh, svh = layer.suh.to(dev), layer.svh.to(dev)
+    runs = []
+    for t in MOE["tokens"]:
+        block = 32 if t * topk < 32 * ne else 128  # few rows per expert: the small block
+        r = synthetic.make_routing(t, ne, topk, block, seed=1202 + t, empty_blocks=0)
+        x = synthetic.make_x(t, hid, seed=1203).to(dev)
+        ids, be = r.sorted_ids.to(dev), r.block_expert.to(dev)
+        xh = torch.empty((2, r.rows, hid), dtype=torch.float16, device=dev)
+        y = torch.empty((r.rows, n), dtype=torch.bfloat16, device=dev)
+        used = int((r.block_expert >= 0).sum())
+        touched = len(set(r.block_expert.tolist()) - {-1})
+        runs.append(dict(t=t, block=block, rows=r.rows, x=x, ids=ids, be=be, xh=xh, y=y, blocks=used,
+                         bytes=touched * expert_bytes, flops=2.0 * t * topk * hid * n))
+
+    def step(it):
+        for run in runs:
+            E.moe_input_transform(run["x"], run["ids"], topk, run["be"], run["block"], suh, out=run["xh"])
+            E.moe_gemm(run["xh"], trs[it % copies], bits, cb, svh, layer.shard_cols, run["be"], run["block"],
+                       out=run["y"])
+
+    for w in range(args.warmup):
+        step(w)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(args.steps):
+        step(s)
+    e1.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    t_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    # per-token-count breakdown, measured separately
+    per = []
+    for run in runs:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        reps = 20
+        ev[0].record()
+        for i in range(reps):
+            E.moe_input_transform(run["x"], run["ids"], topk, run["be"], run["block"], suh, out=run["xh"])
+            E.moe_gemm(run["xh"], trs[i % copies], bits, cb, svh, layer.shard_cols, run["be"], run["block"],
+                       out=run["y"])
+        ev[1].record()
+        torch.cuda.synchronize()
+        t = ev[0].elapsed_time(ev[1]) / 1e3 / reps
+        sol = max(run["bytes"] / (peaks["hbm_gbs"] * 1e9), run["flops"] / (peaks["bf16_tflops"] * 1e12))
+        per.append({"tokens": run["t"], "block": run["block"], "rows": run["rows"], "live_blocks": run["blocks"],
+                    "us": round(t * 1e6, 2), "GBps_touched_experts": round(run["bytes"] / t / 1e9, 1),
+                    "pct_roofline": round(100.0 * sol / t, 2)})
+    sol_step = sum(max(r_["bytes"] / (peaks["hbm_gbs"] * 1e9), r_["flops"] / (peaks["bf16_tflops"] * 1e12))
+                   for r_ in runs)
+    return {
+        "metric": "EXL3 MoE expert gate_up (gathered transform + grouped GEMM) %roofline vs tokens",
+        "value": round(100.0 * sol_step / t_step, 3),
+        "unit": "% of 1-GPU roofline (touched experts' weight bytes at HBM peak, or routed flops at tensor peak)",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16 products, fp32 sums, bf16 out",
+        "data": "synthetic (seeded routing: distinct random top-k experts per token)",
+        "config": {"workload": f"{ne} experts, top-{topk}, hidden {hid}, expert gate_up 2x{inter}, {bits}-bit mcg, "
+                               f"tokens={MOE['tokens']}", "l2": f"weights rotate over {copies} copies"},
+        "sweep": per, "gpu_launches": 2 * len(runs) * args.steps, "clocks": clk,
+        "peaks": {**peaks, "source": peak_src},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="q_proj_sweep", choices=sorted(WORKLOADS) + ["mlp_swiglu"])
+    ap.add_argument("--workload", default="q_proj_sweep", choices=sorted(WORKLOADS) + ["mlp_swiglu", "moe"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--only-m", type=int, default=None,
                     help="restrict the sweep to one batch size (for profiling one launch shape)")
     args = ap.parse_args()
+    if args.workload == "moe":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the single-layer workloads"}))
+            return
+        args.warmup = max(args.warmup, 3)
+        print(json.dumps(run_moe(args)), flush=True)
+        return
     if args.workload == "mlp_swiglu":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the oracle arm covers the single-layer workloads"}))
