@@ -161,6 +161,7 @@ def run_gpu(args, wl_name):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     E.lib()  # fail loudly if the library is missing
+    E.set_autotune(args.autotune)  # the tile shapes are tuned in the first warm-up step
     peaks, peak_src = load_peaks()
 
     layer = synthetic.make_layer(k, widths, bits, cb, seed=1002)
@@ -366,6 +367,7 @@ def run_gpu(args, wl_name):
             "data": "synthetic (seeded; random trellis words, sign*U(0.8,1.2) scales, N(0,1) bf16 activations)",
             "config": {"workload": desc, "k": k, "n": n, "bits": bits, "codebook": ["3inst", "mcg", "mul1"][cb],
                        "m": ms, "split_k": split, "parallelism": f"replicas x{world} (rows independent)",
+                       "tile_shape": "autotuned in warm-up" if args.autotune else "cost model",
                        "l2": f"weights rotate over {copies} copies ({copies * wbytes / 1e6:.0f} MB > 3x L2)"},
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
@@ -696,6 +698,8 @@ def main():
     ap.add_argument("--workload", default="q_proj_sweep", choices=sorted(WORKLOADS) + ["mlp_swiglu", "moe"])
     ap.add_argument("--cpu-seconds", type=float, default=20.0)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--autotune", action="store_true",
+                    help="time every tile shape once per layer shape and batch bucket (in the warm-up)")
     ap.add_argument("--only-m", type=int, default=None,
                     help="restrict the sweep to one batch size (for profiling one launch shape)")
     args = ap.parse_args()

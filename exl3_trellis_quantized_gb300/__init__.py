@@ -8,6 +8,8 @@ PyTorch fallback; if the library is missing every call raises.
 from .binding import (  # noqa: F401
     CODEBOOKS,
     Exl3Error,
+    autotune_entries,
+    clear_autotune,
     device_status,
     gemm,
     gemm_splitk,
@@ -15,6 +17,7 @@ from .binding import (  # noqa: F401
     input_transform_swiglu,
     lib,
     linear,
+    set_autotune,
     moe_gemm,
     moe_input_transform,
     splitk_parts,

@@ -62,6 +62,12 @@ def lib() -> ctypes.CDLL:
     L.exl3_test_gemm_shape.restype = ctypes.c_int
     L.exl3_test_codebook.argtypes = [ctypes.c_int, vp, vp]
     L.exl3_test_unpack.argtypes = [vp, i32, ctypes.c_int, i64, i64, vp, vp]
+    L.exl3_set_autotune.argtypes = [i32]
+    L.exl3_set_autotune.restype = ctypes.c_int
+    L.exl3_clear_autotune.argtypes = []
+    L.exl3_clear_autotune.restype = ctypes.c_int
+    L.exl3_autotune_entries.argtypes = []
+    L.exl3_autotune_entries.restype = i64
     L.exl3_status_string.argtypes = [ctypes.c_int]
     L.exl3_status_string.restype = ctypes.c_char_p
     L.exl3_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -79,6 +85,19 @@ def device_status() -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().exl3_device_status(ctypes.byref(flags)), "exl3_device_status")
     return int(flags.value)
+
+
+def set_autotune(enable: bool) -> None:
+    """Tile-shape autotune: time every shape on a key's first uncaptured call and keep the fastest."""
+    _check(lib().exl3_set_autotune(1 if enable else 0), "exl3_set_autotune")
+
+
+def clear_autotune() -> None:
+    _check(lib().exl3_clear_autotune(), "exl3_clear_autotune")
+
+
+def autotune_entries() -> int:
+    return int(lib().exl3_autotune_entries())
 
 
 def status_string(status: int) -> str:

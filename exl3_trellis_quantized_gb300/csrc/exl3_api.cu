@@ -222,6 +222,19 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
                      "exl3_test_unpack");
 }
 
+exl3_status_t exl3_set_autotune(int32_t enable) {
+  if (enable != 0 && enable != 1) return EXL3_EINVAL;
+  exl3::tc_set_autotune(enable == 1);
+  return EXL3_OK;
+}
+
+exl3_status_t exl3_clear_autotune(void) {
+  exl3::tc_clear_autotune();
+  return EXL3_OK;
+}
+
+int64_t exl3_autotune_entries(void) { return exl3::tc_autotune_entries(); }
+
 const char* exl3_status_string(exl3_status_t status) {
   switch (status) {
     case EXL3_OK: return "ok";

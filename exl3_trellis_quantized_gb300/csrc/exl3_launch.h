@@ -95,6 +95,10 @@ enum class TcShape : int {
 cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream, int shape = -1);
 // Whether tile shape `shape` can run the call described by `args`.
 bool tc_shape_supported(int shape, const GemmArgs& args);
+// Tile-shape autotune (see exl3_tc_host.cu): switch, cache reset, cache size.
+void tc_set_autotune(bool on);
+void tc_clear_autotune();
+int64_t tc_autotune_entries();
 template <int BITS>
 cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, TcShape shape,
                                 cudaStream_t stream);

@@ -3,6 +3,7 @@
 // dispatch.
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
 
 #include "exl3_launch.h"
@@ -195,10 +196,12 @@ bool tc_shape_supported(int shape, const GemmArgs& a) {
   return true;
 }
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream, int forced) {
+namespace {
+
+// One launch of the GEMM kernel with a given tile shape.
+cudaError_t launch_shape(const GemmArgs& a, int bits, int cb, TcShape shape, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  const TcShape shape = forced >= 0 ? (TcShape)forced : choose_shape(a);
   const ShapeDims d = dims_of(shape);
   // rows per activation copy: every allocated row when a stage holds several
   // atoms (their regions sit back to back), else just the rows in use
@@ -218,6 +221,117 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
     case 7: return launch_gemm_tc_bits<7>(maps, p, cb, shape, stream);
     default: return launch_gemm_tc_bits<8>(maps, p, cb, shape, stream);
   }
+}
+
+// Tile-shape autotune (off by default).  A call's key is its device, width,
+// codebook, k, n, shard edges, split-k parts and batch bucket (m <= 32, else
+// the next power of two of m).  On a miss, outside stream capture, every shape
+// that can run the call is launched once to warm up and twice under CUDA
+// events on the caller's stream, and the fastest is kept; every shape gives the
+// same bytes, so the choice never changes a result.  The timing synchronises
+// the host with those events.  Under capture the cost model decides.
+struct TuneKey {
+  int dev, bits, cb, parts, num_shards;
+  int64_t k, n, bucket;
+  int32_t cols[kMaxShards + 1];
+  bool operator<(const TuneKey& o) const {
+    if (dev != o.dev) return dev < o.dev;
+    if (bits != o.bits) return bits < o.bits;
+    if (cb != o.cb) return cb < o.cb;
+    if (parts != o.parts) return parts < o.parts;
+    if (k != o.k) return k < o.k;
+    if (n != o.n) return n < o.n;
+    if (bucket != o.bucket) return bucket < o.bucket;
+    if (num_shards != o.num_shards) return num_shards < o.num_shards;
+    for (int i = 0; i <= num_shards; ++i)
+      if (cols[i] != o.cols[i]) return cols[i] < o.cols[i];
+    return false;
+  }
+};
+std::mutex g_tune_mu;
+bool g_tune_on = false;
+std::map<TuneKey, TcShape> g_tune;
+
+int64_t batch_bucket(int64_t m) {
+  if (m <= 32) return 32;
+  int64_t b = 64;
+  while (b < m) b <<= 1;
+  return b;
+}
+
+// The tuned shape for this call, or the model's when tuning is off, the stream
+// is being captured or the timing fails.
+TcShape tuned_shape(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
+  const TcShape model = choose_shape(a);
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    if (!g_tune_on) return model;
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return model;
+  TuneKey key = {};
+  if (cudaGetDevice(&key.dev) != cudaSuccess) return model;
+  key.bits = bits;
+  key.cb = cb;
+  key.parts = a.parts;
+  key.k = a.k;
+  key.n = a.n;
+  key.bucket = batch_bucket(a.m);
+  key.num_shards = a.num_shards;
+  for (int i = 0; i <= a.num_shards; ++i) key.cols[i] = a.shard_cols[i];
+  {
+    std::lock_guard<std::mutex> lock(g_tune_mu);
+    auto it = g_tune.find(key);
+    if (it != g_tune.end()) return it->second;
+  }
+  cudaEvent_t ev[2];
+  if (cudaEventCreate(&ev[0]) != cudaSuccess) return model;
+  if (cudaEventCreate(&ev[1]) != cudaSuccess) {
+    cudaEventDestroy(ev[0]);
+    return model;
+  }
+  TcShape best = model;
+  float best_ms = 1e30f;
+  for (int s = 0; s <= (int)TcShape::kN128SmallK4; ++s) {
+    if (!tc_shape_supported(s, a)) continue;
+    const TcShape shape = (TcShape)s;
+    bool ok = launch_shape(a, bits, cb, shape, stream) == cudaSuccess;  // warm-up
+    ok = ok && cudaEventRecord(ev[0], stream) == cudaSuccess;
+    for (int r = 0; ok && r < 2; ++r) ok = launch_shape(a, bits, cb, shape, stream) == cudaSuccess;
+    ok = ok && cudaEventRecord(ev[1], stream) == cudaSuccess && cudaEventSynchronize(ev[1]) == cudaSuccess;
+    float ms = 0.f;
+    if (ok && cudaEventElapsedTime(&ms, ev[0], ev[1]) == cudaSuccess && ms < best_ms) {
+      best_ms = ms;
+      best = shape;
+    }
+  }
+  cudaEventDestroy(ev[0]);
+  cudaEventDestroy(ev[1]);
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  g_tune[key] = best;
+  return best;
+}
+
+}  // namespace
+
+void tc_set_autotune(bool on) {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  g_tune_on = on;
+}
+
+void tc_clear_autotune() {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  g_tune.clear();
+}
+
+int64_t tc_autotune_entries() {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  return (int64_t)g_tune.size();
+}
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t stream, int forced) {
+  const TcShape shape = forced >= 0 ? (TcShape)forced : tuned_shape(a, bits, cb, stream);
+  return launch_shape(a, bits, cb, shape, stream);
 }
 
 cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, cudaStream_t stream) {

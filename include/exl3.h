@@ -265,6 +265,27 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
                                    void* stream);
 
 /*
+ * Tile-shape autotune (off by default).  The best tile for a batch size
+ * depends on the layer's shape too, so the shape is timed once per distinct
+ * shape and cached, never while a CUDA graph is being captured, and the cost
+ * model stays the fallback for captured work (cuda-exl3 README, "Where the
+ * time goes").  Here the split-k parts are fixed by (k, n) so that rows stay
+ * byte-equal across batch sizes; only the tile shape is tuned.  When enabled, the first
+ * exl3_gemm / exl3_gemm_splitk call of each key (device, width, codebook, k,
+ * n, shard edges, split parts, batch bucket: m <= 32, else the next power of
+ * two of m) that is not being captured into a CUDA graph times every tile
+ * shape that can run it on the caller's stream (synchronising the host) and
+ * keeps the fastest; later calls of the key use it.  Every shape computes the
+ * same bytes, so tuning never changes a result.  Under capture, or when
+ * disabled, a cost model of measured per-shape rates decides.
+ *   exl3_set_autotune(1 | 0), exl3_clear_autotune(), exl3_autotune_entries()
+ *   (the number of cached keys).
+ */
+exl3_status_t exl3_set_autotune(int32_t enable);
+exl3_status_t exl3_clear_autotune(void);
+int64_t exl3_autotune_entries(void);
+
+/*
  * exl3_device_status -- read and clear the library's device-side error flags.
  * Every wait inside the kernels is bounded; a kernel that gives up sets bit 0
  * (EXL3_DEVERR_WAIT_TIMEOUT) and skips its stores instead of hanging.  This call
