@@ -111,6 +111,12 @@ constexpr double kRel64 = 0.48, kRel32 = 0.43;
 
 constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33;
 
+// Split-k at m <= 128: a 256-column CTA over a k part costs this many 128-column
+// CTAs (decode-bound; its per-stage synchronisation, prologue and epilogue are
+// shared by twice the columns), measured on GB300 (17408 x 5120, 6 bits, 7
+// parts, m = 1 to 128).
+constexpr double kCost256Split = 1.75;
+
 // SMs of the current device, read once per device.
 int64_t sm_count() {
   static std::mutex mu;
@@ -140,7 +146,14 @@ double large_batch_time(int64_t ctas, double cost) {
 }
 
 TcShape choose_shape(const GemmArgs& a) {
-  if (a.parts > 1 && a.m <= 128) return a.m <= 32 ? TcShape::kN128Small : TcShape::kN128;
+  bool edges256 = (a.n % 256) == 0;
+  for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
+  if (a.parts > 1 && a.m <= 128) {
+    // whole waves of 128-column CTAs against fewer, wider ones
+    if (edges256 && large_batch_time(a.n / 256 * a.parts, kCost256Split) < large_batch_time(a.n / 128 * a.parts, 1.0))
+      return TcShape::kN256R2;
+    return a.m <= 32 ? TcShape::kN128Small : TcShape::kN128;
+  }
   if (a.m <= 32) {
     // pick the column width whose grid keeps the most decode throughput busy
     const double r128 = small_batch_rate(a.n / 128, 1.0);
@@ -158,8 +171,6 @@ TcShape choose_shape(const GemmArgs& a) {
   // (5120 x 12288 at 6 bits, 5120 x 34816 at 5 bits, 12288 x 4096 at 5 bits,
   // m = 256 to 4096).  Pair shapes decode half of the columns per CTA; their
   // grid pads the row blocks to an even count.
-  bool edges256 = (a.n % 256) == 0;
-  for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
   // split-k parts multiply every grid
   const int64_t g128 = (a.m + 127) / 128 * a.parts, g256 = (a.m + 255) / 256 * a.parts,
                 g512 = 2 * ((a.m + 511) / 512) * a.parts;
@@ -225,11 +236,15 @@ cudaError_t launch_shape(const GemmArgs& a, int bits, int cb, TcShape shape, cud
 
 // Tile-shape autotune (off by default).  A call's key is its device, width,
 // codebook, k, n, shard edges, split-k parts and batch bucket (m <= 32, else
-// the next power of two of m).  On a miss, outside stream capture, every shape
-// that can run the call is launched once to warm up and twice under CUDA
-// events on the caller's stream, and the fastest is kept; every shape gives the
-// same bytes, so the choice never changes a result.  The timing synchronises
-// the host with those events.  Under capture the cost model decides.
+// the next power of two of m).  On a miss outside stream capture, every shape
+// that can run the call is timed with CUDA events on the caller's stream (the
+// host waits on them): two rounds over the candidates, a warm-up launch in the
+// first, two timed launches in each, a shape's time the lower of its rounds so
+// a clock or power swing during one round does not decide.  The cost model's
+// shape is kept unless another is more than 2% faster.  Every shape gives the
+// same bytes, so the choice never changes a result.  Under capture the cache
+// is read but never filled: a key tuned in an eager warm-up reaches captured
+// work, any other key takes the cost model's shape.
 struct TuneKey {
   int dev, bits, cb, parts, num_shards;
   int64_t k, n, bucket;
@@ -259,16 +274,14 @@ int64_t batch_bucket(int64_t m) {
   return b;
 }
 
-// The tuned shape for this call, or the model's when tuning is off, the stream
-// is being captured or the timing fails.
+// The tuned shape for this call, or the cost model's when tuning is off, the
+// key is untuned under capture, or the timing fails.
 TcShape tuned_shape(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
   const TcShape model = choose_shape(a);
   {
     std::lock_guard<std::mutex> lock(g_tune_mu);
     if (!g_tune_on) return model;
   }
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return model;
   TuneKey key = {};
   if (cudaGetDevice(&key.dev) != cudaSuccess) return model;
   key.bits = bits;
@@ -284,29 +297,35 @@ TcShape tuned_shape(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
     auto it = g_tune.find(key);
     if (it != g_tune.end()) return it->second;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return model;
+  constexpr int kShapes = (int)TcShape::kN128SmallK4 + 1;
+  float best_ms[kShapes];
+  for (int s = 0; s < kShapes; ++s) best_ms[s] = 1e30f;
   cudaEvent_t ev[2];
   if (cudaEventCreate(&ev[0]) != cudaSuccess) return model;
   if (cudaEventCreate(&ev[1]) != cudaSuccess) {
     cudaEventDestroy(ev[0]);
     return model;
   }
-  TcShape best = model;
-  float best_ms = 1e30f;
-  for (int s = 0; s <= (int)TcShape::kN128SmallK4; ++s) {
-    if (!tc_shape_supported(s, a)) continue;
-    const TcShape shape = (TcShape)s;
-    bool ok = launch_shape(a, bits, cb, shape, stream) == cudaSuccess;  // warm-up
-    ok = ok && cudaEventRecord(ev[0], stream) == cudaSuccess;
-    for (int r = 0; ok && r < 2; ++r) ok = launch_shape(a, bits, cb, shape, stream) == cudaSuccess;
-    ok = ok && cudaEventRecord(ev[1], stream) == cudaSuccess && cudaEventSynchronize(ev[1]) == cudaSuccess;
-    float ms = 0.f;
-    if (ok && cudaEventElapsedTime(&ms, ev[0], ev[1]) == cudaSuccess && ms < best_ms) {
-      best_ms = ms;
-      best = shape;
+  for (int round = 0; round < 2; ++round) {
+    for (int s = 0; s < kShapes; ++s) {
+      if (!tc_shape_supported(s, a)) continue;
+      const TcShape shape = (TcShape)s;
+      bool ok = round > 0 || launch_shape(a, bits, cb, shape, stream) == cudaSuccess;  // warm-up
+      ok = ok && cudaEventRecord(ev[0], stream) == cudaSuccess;
+      for (int r = 0; ok && r < 2; ++r) ok = launch_shape(a, bits, cb, shape, stream) == cudaSuccess;
+      ok = ok && cudaEventRecord(ev[1], stream) == cudaSuccess && cudaEventSynchronize(ev[1]) == cudaSuccess;
+      float ms = 0.f;
+      if (ok && cudaEventElapsedTime(&ms, ev[0], ev[1]) == cudaSuccess) best_ms[s] = fminf(best_ms[s], ms);
     }
   }
   cudaEventDestroy(ev[0]);
   cudaEventDestroy(ev[1]);
+  TcShape best = model;
+  const float bar = 0.98f * best_ms[(int)model];
+  for (int s = 0; s < kShapes; ++s)
+    if (best_ms[s] < bar && best_ms[s] < best_ms[(int)best]) best = (TcShape)s;
   std::lock_guard<std::mutex> lock(g_tune_mu);
   g_tune[key] = best;
   return best;

@@ -270,16 +270,20 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
  * shape and cached, never while a CUDA graph is being captured, and the cost
  * model stays the fallback for captured work (cuda-exl3 README, "Where the
  * time goes").  Here the split-k parts are fixed by (k, n) so that rows stay
- * byte-equal across batch sizes; only the tile shape is tuned.  When enabled, the first
- * exl3_gemm / exl3_gemm_splitk call of each key (device, width, codebook, k,
- * n, shard edges, split parts, batch bucket: m <= 32, else the next power of
- * two of m) that is not being captured into a CUDA graph times every tile
- * shape that can run it on the caller's stream (synchronising the host) and
- * keeps the fastest; later calls of the key use it.  Every shape computes the
- * same bytes, so tuning never changes a result.  Under capture, or when
- * disabled, a cost model of measured per-shape rates decides.
- *   exl3_set_autotune(1 | 0), exl3_clear_autotune(), exl3_autotune_entries()
- *   (the number of cached keys).
+ * byte-equal across batch sizes; only the tile shape is tuned.
+ * When enabled, the first uncaptured exl3_gemm / exl3_gemm_splitk call of each
+ * key (device, width, codebook, k, n, shard edges, split parts, batch bucket:
+ * m <= 32, else the next power of two of m) times every tile shape that can
+ * run it on the caller's stream, synchronising the host, and caches the
+ * fastest (the cost model's shape unless another is more than 2% faster).
+ * The timing launches write the call's own y (or acc) several times; the
+ * result is the final launch's, and every shape computes the same bytes, so
+ * tuning never changes a result.  A call under capture uses the cached shape
+ * of its key if there is one (tune in an eager warm-up to reach captured
+ * work), else the cost model's, and never tunes.
+ *   exl3_set_autotune(1 | 0): EXL3_EINVAL for any other value.
+ *   exl3_clear_autotune(): forget every cached key.
+ *   exl3_autotune_entries(): the number of cached keys.
  */
 exl3_status_t exl3_set_autotune(int32_t enable);
 exl3_status_t exl3_clear_autotune(void);

@@ -133,3 +133,13 @@ def test_test_entry_points_reject_invalid(L):
     assert L.exl3_test_codebook(7, v, None) == 1
     assert L.exl3_test_unpack(v, 9, 0, 64, 64, v, None) == 1
     assert L.exl3_test_unpack(v, 3, 0, 40, 64, v, None) == 1
+
+
+def test_autotune_switch(L):
+    """The tuner's switch and cache are host state: no device call is made."""
+    assert L.exl3_set_autotune(2) == 1  # EXL3_EINVAL
+    assert L.exl3_set_autotune(-1) == 1
+    assert L.exl3_set_autotune(1) == 0
+    assert L.exl3_set_autotune(0) == 0
+    assert L.exl3_clear_autotune() == 0
+    assert L.exl3_autotune_entries() == 0

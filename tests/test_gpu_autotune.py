@@ -84,6 +84,16 @@ def test_keys_by_bucket_and_shape():
     assert E.autotune_entries() == 0
 
 
+def _capture(fn):
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+    return graph
+
+
 def test_no_tuning_under_graph_capture():
     k, m, bits, cb = 1024, 48, 5, 2
     tr, suh, svh, cols = _layer(k, [256, 256], bits, cb, seed=7300)
@@ -91,14 +101,26 @@ def test_no_tuning_under_graph_capture():
     xh = E.input_transform(x, suh)
     y_model = E.gemm(xh, tr, bits, cb, svh, cols)
     E.set_autotune(True)
-    stream = torch.cuda.Stream()
     y = torch.empty_like(y_model)
-    stream.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        with torch.cuda.graph(graph, stream=stream):
-            y.copy_(E.gemm(xh, tr, bits, cb, svh, cols))
+    graph = _capture(lambda: E.gemm(xh, tr, bits, cb, svh, cols, out=y))
     assert E.autotune_entries() == 0, "a captured launch must not tune"
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_model.view(torch.int16))
+
+
+def test_eager_tuning_reaches_capture():
+    """A key tuned eagerly is used, not re-tuned, by a captured launch."""
+    k, m, bits, cb = 2048, 16, 3, 0
+    tr, suh, svh, cols = _layer(k, [768], bits, cb, seed=7400)
+    xh = E.input_transform(synthetic.make_x(m, k, seed=7401).to(DEV), suh)
+    y_model = E.gemm(xh, tr, bits, cb, svh, cols)
+    E.set_autotune(True)
+    E.gemm(xh, tr, bits, cb, svh, cols)  # eager warm-up tunes the key
+    assert E.autotune_entries() == 1
+    y = torch.empty_like(y_model)
+    graph = _capture(lambda: E.gemm(xh, tr, bits, cb, svh, cols, out=y))
+    assert E.autotune_entries() == 1
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y_model.view(torch.int16))
