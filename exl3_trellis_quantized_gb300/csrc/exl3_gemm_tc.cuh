@@ -3,11 +3,12 @@
 // One CTA owns BN output columns and RG*128 rows over the whole k extent (or
 // over one shape-fixed part of k under split-k).  Owning all of k lets a block
 // stream its share of the trellis a single time and apply the output Hadamard
-// and svh in its epilogue (cuda-exl3 README, "Why custom kernels").  When
-// BN < 128 a thread-block cluster of 128/BN CTAs spans one 128-column Hadamard
-// block: each CTA accumulates its own columns and the epilogue reads the
-// partners' fp32 tiles through distributed shared memory, so the arithmetic is
-// the same whatever BN is.  With PAIR = 2 two CTAs that own the same columns and
+// and svh in its epilogue (cuda-exl3 README, "Why custom kernels").  When BN
+// is not a multiple of 128, a thread-block cluster of 128/gcd(BN, 128) CTAs
+// spans whole 128-column Hadamard blocks (32 columns: 4 CTAs over one block;
+// 96 columns: 4 CTAs over three): each CTA accumulates its own columns and the
+// epilogue reads the partners' fp32 tiles through distributed shared memory,
+// so the arithmetic is the same whatever BN is.  With PAIR = 2 two CTAs that own the same columns and
 // neighbouring rows form a cluster: each decodes half of the columns and copies
 // its half of the decoded operand into the partner's shared memory, so every
 // decoded weight feeds 2*RG*128 rows.
@@ -57,9 +58,11 @@ constexpr int kTcFirstDecoder = 4;  // warps 0..3: trellis producer, MMA issuer,
 constexpr int kTcThreads = 32 * (kTcFirstDecoder + kTcDecodeWarps);
 constexpr int kTcSmemBudget = 227 * 1024;
 
+constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+
 template <int BITS, int BN, int RG, int KA, int XR, int PAIR>
 struct TcCfg {
-  static constexpr int kClusterX = BN < 128 ? 128 / BN : 1;  // CTAs spanning a Hadamard block
+  static constexpr int kClusterX = 128 / gcd_int(BN, 128);  // CTAs spanning whole Hadamard blocks
   static constexpr int kCluster = kClusterX * PAIR;
   static constexpr int kXAtom = XR * 128;                     // one atom of one row group
   static constexpr int kXSlot = RG * KA * kXAtom;             // activations of a stage
@@ -462,7 +465,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     const uint32_t rank = (CLX > 1) ? cluster_ctarank() : 0u;
     const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
-    constexpr int kSpan = BN < 128 ? 128 : BN;
+    constexpr int kSpan = CLX * BN;  // whole 128-column blocks
     for (int r = 0; r < RG; ++r) {
       // 1. tensor memory -> zs[128][BN].  Each thread holds one row's 32
       // consecutive columns after a load and runs the Hadamard stages of
@@ -588,6 +591,7 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN128R2P: return launch_tc_variant<BITS, CB, 128, 2, 1, 128, 2>(maps, p, stream);
     case TcShape::kN256R2P: return launch_tc_variant<BITS, CB, 256, 2, 1, 128, 2>(maps, p, stream);
     case TcShape::kN128SmallK4: return launch_tc_variant<BITS, CB, 128, 1, 4, 32>(maps, p, stream);
+    case TcShape::kN96SmallK4: return launch_tc_variant<BITS, CB, 96, 1, 4, 32>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

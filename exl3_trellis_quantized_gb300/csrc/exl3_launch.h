@@ -74,7 +74,8 @@ struct TcMaps {
 };
 // Tile shapes of the tcgen05 GEMM: columns per CTA (BN), row groups of 128
 // (RG), 64-wide k atoms per pipeline stage (KA) and activation rows held per
-// atom (XR).  Shapes with BN < 128 run as clusters of 128/BN CTAs; pair shapes
+// atom (XR).  Shapes whose BN is not a multiple of 128 run as clusters of
+// 128/gcd(BN, 128) CTAs that span whole Hadamard blocks; pair shapes
 // (P) as clusters of two CTAs on neighbouring rows that decode half of the
 // columns each and share the decoded operand.
 enum class TcShape : int {
@@ -87,6 +88,9 @@ enum class TcShape : int {
   kN128R2P,    // BN=128, RG=2, KA=1, XR=128, pair (large m)
   kN256R2P,    // BN=256, RG=2, KA=1, XR=128, pair (large m, 256-aligned shard edges)
   kN128SmallK4,  // BN=128, RG=1, KA=4, XR=32  (m <= 32, wide layers, even k/128, no split-k)
+  kN96SmallK4,   // BN=96,  RG=1, KA=4, XR=32  (m <= 32, n and shard edges multiples of 384, even k/128,
+                 //                             no split-k; clusters of 4 CTAs over 3 Hadamard blocks)
+  kLast = kN96SmallK4,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

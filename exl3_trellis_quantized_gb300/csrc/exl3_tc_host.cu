@@ -95,6 +95,7 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN128R2P: return {128, 1, 128, 2};
     case TcShape::kN256R2P: return {256, 1, 128, 2};
     case TcShape::kN128SmallK4: return {128, 4, 32, 1};
+    case TcShape::kN96SmallK4: return {96, 4, 32, 1};
     default: return {256, 1, 128, 1};
   }
 }
@@ -104,10 +105,10 @@ ShapeDims dims_of(TcShape s) {
 // trades parallelism (small batches need many CTAs to reach every SM) against
 // reuse of each decoded tile across rows (large batches).
 // Decode throughput a small-batch CTA reaches on its SM relative to a
-// 128-column CTA, measured on GB300 (q_proj-like layer, m = 16): narrow strips
-// spend more of each SM on the cluster, per-stage synchronisation and the
-// tensor core's 128-row operand reads.
-constexpr double kRel64 = 0.48, kRel32 = 0.43;
+// 128-column CTA, measured on GB300 (q_proj-like layer, m = 1 to 32): narrow
+// strips spend more of each SM on the cluster, per-stage synchronisation and
+// the tensor core's 128-row operand reads.
+constexpr double kRel64 = 0.48, kRel32 = 0.43, kRel96 = 0.81;
 
 constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33;
 
@@ -145,9 +146,25 @@ double large_batch_time(int64_t ctas, double cost) {
   return (double)((ctas + sms - 1) / sms) * cost;
 }
 
+int64_t lcm_128(int64_t bn) {
+  int64_t x = bn, y = 128;
+  while (y != 0) {
+    const int64_t t = x % y;
+    x = y;
+    y = t;
+  }
+  return bn / x * 128;
+}
+
+bool edges_multiple_of(const GemmArgs& a, int64_t span) {
+  if (a.n % span != 0) return false;
+  for (int i = 0; i <= a.num_shards; ++i)
+    if (a.shard_cols[i] % span != 0) return false;
+  return true;
+}
+
 TcShape choose_shape(const GemmArgs& a) {
-  bool edges256 = (a.n % 256) == 0;
-  for (int i = 0; i <= a.num_shards; ++i) edges256 = edges256 && (a.shard_cols[i] % 256) == 0;
+  const bool edges256 = edges_multiple_of(a, 256);
   if (a.parts > 1 && a.m <= 128) {
     // whole waves of 128-column CTAs against fewer, wider ones
     if (edges256 && large_batch_time(a.n / 256 * a.parts, kCost256Split) < large_batch_time(a.n / 128 * a.parts, 1.0))
@@ -159,10 +176,14 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r128 = small_batch_rate(a.n / 128, 1.0);
     const double r64 = small_batch_rate(a.n / 64, kRel64);
     // 32-column strips use 4 k atoms per stage: k must hold an even number of 128-blocks
-    const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
+    const bool k4 = (a.k / 128) % 2 == 0;
+    const double r32 = k4 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
+    // 96-column strips: clusters of four over three Hadamard blocks
+    const double r96 = k4 && edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
     // four k atoms per stage halve the per-stage synchronisation (k must hold
     // an even number of 128-blocks)
-    if (r128 >= r64 && r128 >= r32) return (a.k / 128) % 2 == 0 ? TcShape::kN128SmallK4 : TcShape::kN128Small;
+    if (r128 >= r96 && r128 >= r64 && r128 >= r32) return k4 ? TcShape::kN128SmallK4 : TcShape::kN128Small;
+    if (r96 >= r64 && r96 >= r32) return TcShape::kN96SmallK4;
     return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
   }
   if (a.m <= 128) return TcShape::kN128;
@@ -194,17 +215,14 @@ TcShape choose_shape(const GemmArgs& a) {
 }  // namespace
 
 bool tc_shape_supported(int shape, const GemmArgs& a) {
-  if (shape < 0 || shape > (int)TcShape::kN128SmallK4) return false;
+  if (shape < 0 || shape > (int)TcShape::kLast) return false;
   const TcShape s = (TcShape)shape;
   const ShapeDims d = dims_of(s);
   if (d.xr < 128 && a.m > d.xr) return false;  // small-batch shapes hold XR rows
   if (d.ka == 4 && ((a.k / 128) % 2 != 0 || a.parts > 1)) return false;
-  if (d.bn == 256) {
-    if (a.n % 256 != 0) return false;
-    for (int i = 0; i <= a.num_shards; ++i)
-      if (a.shard_cols[i] % 256 != 0) return false;
-  }
-  return true;
+  // n and every shard edge fall on whole CTA spans: lcm(BN, 128) columns (a
+  // cluster's span when BN is not a multiple of 128)
+  return edges_multiple_of(a, lcm_128(d.bn));
 }
 
 namespace {
@@ -299,7 +317,7 @@ TcShape tuned_shape(const GemmArgs& a, int bits, int cb, cudaStream_t stream) {
   }
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) return model;
-  constexpr int kShapes = (int)TcShape::kN128SmallK4 + 1;
+  constexpr int kShapes = (int)TcShape::kLast + 1;
   float best_ms[kShapes];
   for (int s = 0; s < kShapes; ++s) best_ms[s] = 1e30f;
   cudaEvent_t ev[2];

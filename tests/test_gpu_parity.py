@@ -192,6 +192,7 @@ TILE_CASES = [
     (2048, [256, 256], 6, 2),
     (1152, [384, 128], 2, 0),  # an odd number of 128-blocks of k; 128-aligned shard edges
     (1024, [1024], 8, 1),
+    (2048, [384, 384], 4, 2),  # 384-aligned edges: 96-column strips over two shards
 ]
 
 
@@ -224,7 +225,7 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     # the cases reach every shape that their sizes allow
     need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     if not split and (k // 128) % 2 == 0:
-        need |= {0, 8}
+        need |= {0, 8} | ({9} if all(w % 384 == 0 for w in widths) else set())
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
 
 
