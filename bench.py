@@ -234,12 +234,57 @@ def run_gpu(args, wl_name):
 
     # per-batch-size breakdown, measured separately (same launches, events around each)
     reps = max(3, min(args.steps, 50))
+    per_m_samples = [[] for _ in ms]
     for _ in range(reps):
         step(per_m)
         torch.cuda.synchronize()
         for i in range(len(ms)):
-            per_m_ms[i] += per_m[i][0].elapsed_time(per_m[i][1])
+            t_ms = per_m[i][0].elapsed_time(per_m[i][1])
+            per_m_ms[i] += t_ms
+            per_m_samples[i].append(t_ms)
     per_m_s = [v / reps / 1e3 for v in per_m_ms]
+
+    def pct(vals, q):
+        v = sorted(vals)
+        return v[min(len(v) - 1, int(q * (len(v) - 1) + 0.5))]
+
+    # The same linears replayed from a CUDA graph: `reps` back-to-back linears
+    # of one batch size (weights rotating) captured once, so the time excludes
+    # host launch overhead (small layers at small m are launch-bound otherwise).
+    graph_s = []
+    cap_stream = torch.cuda.Stream(dev)
+    cap_stream.wait_stream(stream)
+    for i in range(len(ms)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap_stream):
+            with torch.cuda.graph(g, stream=cap_stream):
+                for r in range(reps):
+                    one_linear(i, r + i)
+        g.replay()
+        torch.cuda.synchronize()
+        e0g, e1g = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0g.record(stream)
+        for _ in range(3):
+            g.replay()
+        e1g.record(stream)
+        torch.cuda.synchronize()
+        graph_s.append(e0g.elapsed_time(e1g) / 1e3 / (3 * reps))
+        del g
+
+    # A bandwidth ruler in the same process: a device-to-device copy of 2 GiB.
+    # A kernel reading above it flags a timing artefact.
+    ruler_src = torch.empty(1 << 30, dtype=torch.int16, device=dev)
+    ruler_dst = torch.empty_like(ruler_src)
+    ruler_dst.copy_(ruler_src)
+    torch.cuda.synchronize()
+    er0, er1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    er0.record(stream)
+    for _ in range(5):
+        ruler_dst.copy_(ruler_src)
+    er1.record(stream)
+    torch.cuda.synchronize()
+    ruler_gbps = 5 * 2 * ruler_src.numel() * 2 / (er0.elapsed_time(er1) / 1e3) / 1e9
+    del ruler_src, ruler_dst
 
     sol_step = sum(sol_seconds(m, k, n, bits, peaks)[0] for m in ms)
     value = 100.0 * sol_step * args.steps * world / elapsed
@@ -281,7 +326,9 @@ def run_gpu(args, wl_name):
     for i, m in enumerate(ms):
         t = per_m_s[i]
         sol, b = sol_seconds(m, k, n, bits, peaks)
-        sweep.append({"m": m, "us": round(t * 1e6, 2), "gemm_us": round(gemm_s[i] * 1e6, 2),
+        sweep.append({"m": m, "us": round(t * 1e6, 2), "us_p10": round(pct(per_m_samples[i], 0.1) * 1e3, 2),
+                      "us_p90": round(pct(per_m_samples[i], 0.9) * 1e3, 2), "graph_us": round(graph_s[i] * 1e6, 2),
+                      "gemm_us": round(gemm_s[i] * 1e6, 2),
                       "GBps": round(k * n * bits / 8 / t / 1e9, 1),
                       "TFLOPS": round(2.0 * m * k * n / t / 1e12, 2),
                       "pct_roofline": round(100.0 * sol / t, 2), "bound": b})
@@ -375,6 +422,7 @@ def run_gpu(args, wl_name):
             "roofline": roofline,
             "sweep": sweep,
             "clocks": clk,
+            "ruler": {"copy_gbps": round(ruler_gbps, 1), "of_hbm_peak": round(ruler_gbps / peaks["hbm_gbs"], 3)},
             "cpu_baseline": cpu,
             "peaks": {**peaks, "source": peak_src},
         }
