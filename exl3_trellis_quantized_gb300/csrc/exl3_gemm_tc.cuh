@@ -152,11 +152,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t c0 = (int64_t)blockIdx.x * BN;
-  const int64_t row0 = (int64_t)blockIdx.y * (MOE ? XR : 128 * RG);
-  const int part = (int)blockIdx.z;
-  // rank within the pair (cluster dims {1, 2, 1})
+  // A pair is a cluster {2, 1, 1}: blockIdx.x = 2 * pair tile + rank, pair
+  // tiles numbered row pair major (a.tile_cols per row pair).
   const uint32_t prank = PAIR > 1 ? cluster_ctarank() : 0u;
+  int64_t c0, row0;
+  if constexpr (PAIR > 1) {
+    const int64_t t = (int64_t)(blockIdx.x >> 1);
+    const int64_t rp = t / a.tile_cols;
+    c0 = a.col_base + (t - rp * a.tile_cols) * BN;
+    row0 = a.row_base + (rp * 2 + prank) * (128 * RG);
+  } else {
+    c0 = a.col_base + (int64_t)blockIdx.x * BN;
+    row0 = (MOE ? 0 : a.row_base) + (int64_t)blockIdx.y * (MOE ? XR : 128 * RG);
+  }
+  const int part = (int)blockIdx.z;
   // this CTA's k range in 64-wide atoms: whole 128-row blocks of k per part
   const int64_t kb0 = (int64_t)part * (a.k >> 7) / a.parts * 2;
   const int64_t kb1 = (int64_t)(part + 1) * (a.k >> 7) / a.parts * 2;
@@ -231,6 +240,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // for it here.  Everything else this kernel reads before the wait (the
       // trellis, svh) is weights, which no kernel of this library writes.
       pdl_wait();
+      // a split launch's tail may now be scheduled onto SMs as they free up
+      if (a.trigger_dependents) pdl_launch_dependents();
       const uint32_t tx = (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
       int s = 0;
       uint32_t ph = 0;
@@ -560,15 +571,19 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
   }
   cudaLaunchConfig_t cfg = {};
   // a pair's second CTA may own only rows past m: it still decodes its half
-  const int64_t row_blocks = MOE ? p.a.m / XR : (p.a.m + 128 * RG - 1) / (128 * RG);
-  cfg.gridDim = dim3((unsigned)(p.a.n / BN), (unsigned)((row_blocks + PAIR - 1) / PAIR * PAIR), (unsigned)p.a.parts);
+  if (PAIR > 1) {
+    cfg.gridDim = dim3((unsigned)(2 * p.a.pair_tiles), 1u, (unsigned)p.a.parts);
+  } else {
+    const int64_t row_blocks = MOE ? p.a.m / XR : (p.a.m - p.a.row_base + 128 * RG - 1) / (128 * RG);
+    cfg.gridDim = dim3((unsigned)((p.a.n - p.a.col_base) / BN), (unsigned)row_blocks, (unsigned)p.a.parts);
+  }
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C::kClusterX;
-  attr[0].val.clusterDim.y = PAIR;
+  attr[0].val.clusterDim.x = C::kClusterX * PAIR;  // strips (BN < 128) and pairs never combine
+  attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   // may start while the previous kernel (the input transform) still runs;
   // the activation producer waits for it (pdl_wait) before reading xh

@@ -36,6 +36,15 @@ struct GemmArgs {
   // grouped (mixture-of-experts) GEMM only: expert of each row block, or -1
   const int32_t* block_expert;
   int32_t num_experts;
+  // Tile placement of one launch (zero: the whole output).  CTAs cover rows
+  // from row_base and columns from col_base; pair shapes number their pair
+  // tiles linearly, row pair major with tile_cols column tiles per row pair,
+  // and launch pair_tiles of them.  trigger_dependents: let the next launch
+  // in the stream start once every CTA has its activations (the tail of a
+  // split launch, see exl3_tc_host.cu).
+  int64_t row_base, col_base;
+  int32_t tile_cols, pair_tiles;
+  int32_t trigger_dependents;
 };
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,

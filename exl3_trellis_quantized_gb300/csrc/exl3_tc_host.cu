@@ -82,21 +82,21 @@ cudaError_t make_moe_trellis_map(CUtensorMap* map, const int16_t* trellis, int64
 }
 
 struct ShapeDims {
-  int bn, ka, xr, pair;
+  int bn, ka, xr, pair, rg;
 };
 
 ShapeDims dims_of(TcShape s) {
   switch (s) {
-    case TcShape::kN32Small: return {32, 4, 32, 1};
-    case TcShape::kN64Small: return {64, 2, 32, 1};
-    case TcShape::kN128Small: return {128, 2, 32, 1};
-    case TcShape::kN128: return {128, 2, 128, 1};
-    case TcShape::kN128R2: return {128, 1, 128, 1};
-    case TcShape::kN128R2P: return {128, 1, 128, 2};
-    case TcShape::kN256R2P: return {256, 1, 128, 2};
-    case TcShape::kN128SmallK4: return {128, 4, 32, 1};
-    case TcShape::kN96SmallK4: return {96, 4, 32, 1};
-    default: return {256, 1, 128, 1};
+    case TcShape::kN32Small: return {32, 4, 32, 1, 1};
+    case TcShape::kN64Small: return {64, 2, 32, 1, 1};
+    case TcShape::kN128Small: return {128, 2, 32, 1, 1};
+    case TcShape::kN128: return {128, 2, 128, 1, 1};
+    case TcShape::kN128R2: return {128, 1, 128, 1, 2};
+    case TcShape::kN128R2P: return {128, 1, 128, 2, 2};
+    case TcShape::kN256R2P: return {256, 1, 128, 2, 2};
+    case TcShape::kN128SmallK4: return {128, 4, 32, 1, 1};
+    case TcShape::kN96SmallK4: return {96, 4, 32, 1, 1};
+    default: return {256, 1, 128, 1, 2};
   }
 }
 
@@ -163,6 +163,64 @@ bool edges_multiple_of(const GemmArgs& a, int64_t span) {
   return true;
 }
 
+// Pair launches split off their partial last wave.  A pair shape's grid of C
+// CTAs fills ceil(C / SMs) waves; when the last is partial its R CTAs (R / 2
+// pair tiles, the last ones in row-pair-major order, so the final columns of
+// the final row pair) can instead run as a second launch of smaller tiles
+// that spread over the whole GPU.  Every shape computes each element with the
+// same k16 steps, so the split changes no byte.  The plan is taken when the
+// smaller tiles' waves cost less than the pair wave they replace (costs as in
+// choose_shape).
+struct TailPlan {
+  bool split = false;
+  int64_t primary_tiles = 0;  // pair tiles of the first launch
+  int64_t row_base = 0, col_base = 0;
+  TcShape tail = TcShape::kN128;
+  double time = 0.0;  // modelled time of both launches
+};
+
+TailPlan plan_tail(const GemmArgs& a, TcShape shape) {
+  const ShapeDims d = dims_of(shape);
+  TailPlan t;
+  const int64_t sms = sm_count();
+  const int64_t ncol = a.n / d.bn, rows_per_tile = 2 * 128 * d.rg;
+  const int64_t nrp = (a.m + rows_per_tile - 1) / rows_per_tile;
+  const int64_t ctas = 2 * ncol * nrp * a.parts;
+  const double cost = d.bn == 256 ? kCost256P : kCost128P;
+  t.time = large_batch_time(ctas, cost);
+  const int64_t rem = ctas % sms;
+  const int64_t tail_tiles = rem / 2;
+  if (a.parts != 1 || sms % 2 != 0 || ctas <= sms || rem == 0 || tail_tiles > ncol) return t;
+  GemmArgs ta = a;
+  ta.row_base = (nrp - 1) * rows_per_tile;
+  ta.col_base = (ncol - tail_tiles) * d.bn;
+  const int64_t rows = a.m - ta.row_base, cols = tail_tiles * d.bn;
+  struct Option {
+    TcShape shape;
+    int64_t rows_per_cta, bn;
+    double cost;
+  };
+  const Option opts[3] = {{TcShape::kN128, 128, 128, kCost128},
+                          {TcShape::kN128R2, 256, 128, 1.0},
+                          {TcShape::kN256R2, 256, 256, kCost256}};
+  double best = 1e300;
+  for (const Option& o : opts) {
+    if (cols % o.bn != 0 || ta.col_base % o.bn != 0 || !tc_shape_supported((int)o.shape, ta)) continue;
+    const double tt = large_batch_time((rows + o.rows_per_cta - 1) / o.rows_per_cta * (cols / o.bn), o.cost);
+    if (tt < best) {
+      best = tt;
+      t.tail = o.shape;
+    }
+  }
+  if (best >= 0.95 * cost) return t;
+  t.split = true;
+  t.primary_tiles = ctas / 2 - tail_tiles;
+  t.row_base = ta.row_base;
+  t.col_base = ta.col_base;
+  t.time = large_batch_time(ctas - rem, cost) + best;
+  return t;
+}
+
 TcShape choose_shape(const GemmArgs& a) {
   const bool edges256 = edges_multiple_of(a, 256);
   if (a.parts > 1 && a.m <= 128) {
@@ -191,10 +249,10 @@ TcShape choose_shape(const GemmArgs& a) {
   // relative to a 256-row, 128-column CTA over the same k, measured on GB300
   // (5120 x 12288 at 6 bits, 5120 x 34816 at 5 bits, 12288 x 4096 at 5 bits,
   // m = 256 to 4096).  Pair shapes decode half of the columns per CTA; their
-  // grid pads the row blocks to an even count.
+  // grid pads the row blocks to an even count, and a partial last wave may be
+  // split off (plan_tail).
   // split-k parts multiply every grid
-  const int64_t g128 = (a.m + 127) / 128 * a.parts, g256 = (a.m + 255) / 256 * a.parts,
-                g512 = 2 * ((a.m + 511) / 512) * a.parts;
+  const int64_t g128 = (a.m + 127) / 128 * a.parts, g256 = (a.m + 255) / 256 * a.parts;
   struct Option {
     TcShape shape;
     double time;
@@ -202,9 +260,9 @@ TcShape choose_shape(const GemmArgs& a) {
   const Option opts[5] = {
       {TcShape::kN128R2, large_batch_time(a.n / 128 * g256, 1.0)},
       {TcShape::kN128, large_batch_time(a.n / 128 * g128, kCost128)},
-      {TcShape::kN128R2P, large_batch_time(a.n / 128 * g512, kCost128P)},
+      {TcShape::kN128R2P, plan_tail(a, TcShape::kN128R2P).time},
       {TcShape::kN256R2, edges256 ? large_batch_time(a.n / 256 * g256, kCost256) : 1e300},
-      {TcShape::kN256R2P, edges256 ? large_batch_time(a.n / 256 * g512, kCost256P) : 1e300},
+      {TcShape::kN256R2P, edges256 ? plan_tail(a, TcShape::kN256R2P).time : 1e300},
   };
   Option best = opts[0];
   for (const Option& o : opts)
@@ -227,11 +285,17 @@ bool tc_shape_supported(int shape, const GemmArgs& a) {
 
 namespace {
 
-// One launch of the GEMM kernel with a given tile shape.
-cudaError_t launch_shape(const GemmArgs& a, int bits, int cb, TcShape shape, cudaStream_t stream) {
+// One launch of the GEMM kernel with a given tile shape over the rows and
+// columns from a.row_base / a.col_base (all pair tiles unless a.pair_tiles).
+cudaError_t launch_one(const GemmArgs& a, int bits, int cb, TcShape shape, cudaStream_t stream) {
   TcParams p;
   p.a = a;
   const ShapeDims d = dims_of(shape);
+  p.a.tile_cols = (int32_t)((a.n - a.col_base) / d.bn);
+  if (d.pair > 1 && p.a.pair_tiles == 0) {
+    const int64_t rows_per_tile = 2 * 128 * d.rg;
+    p.a.pair_tiles = (int32_t)((a.m - a.row_base + rows_per_tile - 1) / rows_per_tile * p.a.tile_cols);
+  }
   // rows per activation copy: every allocated row when a stage holds several
   // atoms (their regions sit back to back), else just the rows in use
   p.box_rows = d.ka > 1 ? d.xr : (a.m >= d.xr ? d.xr : (int)((a.m + 7) / 8 * 8));
@@ -250,6 +314,28 @@ cudaError_t launch_shape(const GemmArgs& a, int bits, int cb, TcShape shape, cud
     case 7: return launch_gemm_tc_bits<7>(maps, p, cb, shape, stream);
     default: return launch_gemm_tc_bits<8>(maps, p, cb, shape, stream);
   }
+}
+
+// The GEMM with a given tile shape: one launch, or for a pair shape whose
+// last wave is better split off, the whole waves of pair tiles followed by a
+// launch of smaller tiles over the rest (plan_tail).  The second launch may
+// be scheduled as soon as every CTA of the first has its activations.
+cudaError_t launch_shape(const GemmArgs& a, int bits, int cb, TcShape shape, cudaStream_t stream) {
+  if (dims_of(shape).pair > 1) {
+    const TailPlan t = plan_tail(a, shape);
+    if (t.split) {
+      GemmArgs first = a;
+      first.pair_tiles = (int32_t)t.primary_tiles;
+      first.trigger_dependents = 1;
+      cudaError_t e = launch_one(first, bits, cb, shape, stream);
+      if (e != cudaSuccess) return e;
+      GemmArgs rest = a;
+      rest.row_base = t.row_base;
+      rest.col_base = t.col_base;
+      return launch_one(rest, bits, cb, t.tail, stream);
+    }
+  }
+  return launch_one(a, bits, cb, shape, stream);
 }
 
 // Tile-shape autotune (off by default).  A call's key is its device, width,

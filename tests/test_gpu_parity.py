@@ -311,3 +311,36 @@ def test_full_size_sampled(name, k, widths, bits, cb, m, split):
     assert not torch.isnan(y.float()).any()
     if split:
         assert not acc.any()
+
+
+SPLIT_CASES = [
+    # k, shard widths, bits, codebook, m: pair launches whose partial last wave
+    # is split off into a second launch of smaller tiles on 152 SMs
+    (256, [12288], 4, 1, 1024),  # 192 pair CTAs: 40 of them become 256-row x 128-column tiles
+    (256, [10240, 2048], 3, 0, 1024),  # the split-off columns span both shards
+    (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 128 x 128 tiles
+]
+
+
+@pytest.mark.parametrize("k,widths,bits,cb,m", SPLIT_CASES, ids=[f"{c[1]}m{c[4]}" for c in SPLIT_CASES])
+def test_split_last_wave_byte_equal(k, widths, bits, cb, m):
+    """A pair launch with its last wave split off gives the bytes of a single
+    launch of one tile shape, and the oracle's values in the split-off region."""
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=4400 + m + bits)
+    tr, suh, svh = _dev(layer)
+    n = layer.n
+    x = synthetic.make_x(m, k, seed=4401)
+    xh = E.input_transform(x.to(DEV), suh)
+    single = B.test_gemm_shape(3, xh, tr, bits, cb, svh, layer.shard_cols)  # 128 x 128 tiles, one launch
+    assert single is not None
+    for shape in (6, 7, None):  # both pair shapes, and the library's own choice
+        got = (E.gemm(xh, tr, bits, cb, svh, layer.shard_cols) if shape is None
+               else B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols))
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), single.view(torch.int16)), f"shape {shape}: bytes differ"
+    # the split-off region is the last columns of the last 512 rows
+    blocks = [0, n // 128 // 2, n // 128 - 1]
+    rows = np.r_[0:8, m - 8:m]
+    ref = _oracle(x[rows], layer, blocks)
+    got = _np(single)[rows].reshape(len(rows), n // 128, 128)[:, blocks].reshape(len(rows), -1)
+    _assert_columns(got, ref)
