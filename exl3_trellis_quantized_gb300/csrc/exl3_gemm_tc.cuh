@@ -607,6 +607,8 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN256R2P: return launch_tc_variant<BITS, CB, 256, 2, 1, 128, 2>(maps, p, stream);
     case TcShape::kN128SmallK4: return launch_tc_variant<BITS, CB, 128, 1, 4, 32>(maps, p, stream);
     case TcShape::kN96SmallK4: return launch_tc_variant<BITS, CB, 96, 1, 4, 32>(maps, p, stream);
+    case TcShape::kN96: return launch_tc_variant<BITS, CB, 96, 1, 2, 128>(maps, p, stream);
+    case TcShape::kN96R2: return launch_tc_variant<BITS, CB, 96, 2, 2, 128>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

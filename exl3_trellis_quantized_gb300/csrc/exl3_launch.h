@@ -99,7 +99,9 @@ enum class TcShape : int {
   kN128SmallK4,  // BN=128, RG=1, KA=4, XR=32  (m <= 32, wide layers, even k/128, no split-k)
   kN96SmallK4,   // BN=96,  RG=1, KA=4, XR=32  (m <= 32, n and shard edges multiples of 384, even k/128,
                  //                             no split-k; clusters of 4 CTAs over 3 Hadamard blocks)
-  kLast = kN96SmallK4,
+  kN96,          // BN=96,  RG=1, KA=2, XR=128 (n and shard edges multiples of 384)
+  kN96R2,        // BN=96,  RG=2, KA=2, XR=128 (n and shard edges multiples of 384)
+  kLast = kN96R2,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

@@ -96,6 +96,8 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN256R2P: return {256, 1, 128, 2, 2};
     case TcShape::kN128SmallK4: return {128, 4, 32, 1, 1};
     case TcShape::kN96SmallK4: return {96, 4, 32, 1, 1};
+    case TcShape::kN96: return {96, 2, 128, 1, 1};
+    case TcShape::kN96R2: return {96, 2, 128, 1, 2};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -109,8 +111,11 @@ ShapeDims dims_of(TcShape s) {
 // strips spend more of each SM on the cluster, per-stage synchronisation and
 // the tensor core's 128-row operand reads.
 constexpr double kRel64 = 0.48, kRel32 = 0.43, kRel96 = 0.81;
+// The same for the full-row (128-row) tiles at 32 < m <= 128: 96 columns
+// against 128 (5120 x 12288, m = 48 to 128).
+constexpr double kRel96Full = 0.76;
 
-constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33;
+constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33, kCost96R2 = 0.91;
 
 // Split-k at m <= 128: a 256-column CTA over a k part costs this many 128-column
 // CTAs (decode-bound; its per-stage synchronisation, prologue and epilogue are
@@ -244,7 +249,13 @@ TcShape choose_shape(const GemmArgs& a) {
     if (r96 >= r64 && r96 >= r32) return TcShape::kN96SmallK4;
     return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
   }
-  if (a.m <= 128) return TcShape::kN128;
+  const bool edges384 = edges_multiple_of(a, 384);
+  if (a.m <= 128) {
+    // as for small batches: 96-column tiles put a 96-block layer on 128 SMs
+    const double r128 = small_batch_rate(a.n / 128, 1.0);
+    const double r96 = edges384 ? small_batch_rate(a.n / 96, kRel96Full) : 0.0;
+    return r96 > r128 ? TcShape::kN96 : TcShape::kN128;
+  }
   // Larger batches: least estimated time over whole waves.  Per-CTA costs are
   // relative to a 256-row, 128-column CTA over the same k, measured on GB300
   // (5120 x 12288 at 6 bits, 5120 x 34816 at 5 bits, 12288 x 4096 at 5 bits,
@@ -257,8 +268,9 @@ TcShape choose_shape(const GemmArgs& a) {
     TcShape shape;
     double time;
   };
-  const Option opts[5] = {
+  const Option opts[6] = {
       {TcShape::kN128R2, large_batch_time(a.n / 128 * g256, 1.0)},
+      {TcShape::kN96R2, edges384 ? large_batch_time(a.n / 96 * g256, kCost96R2) : 1e300},
       {TcShape::kN128, large_batch_time(a.n / 128 * g128, kCost128)},
       {TcShape::kN128R2P, plan_tail(a, TcShape::kN128R2P).time},
       {TcShape::kN256R2, edges256 ? large_batch_time(a.n / 256 * g256, kCost256) : 1e300},

@@ -255,11 +255,13 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
  *     7 = pair of 256-column x 256-row CTAs (edges multiples of 256),
  *     8 = 128 columns, four k atoms per stage (m <= 32, k/128 even, no split-k),
  *     9 = 96-column strips in clusters of four CTAs over three Hadamard blocks
- *         (m <= 32, k/128 even, no split-k, n and shard edges multiples of 384).
+ *         (m <= 32, k/128 even, no split-k, n and shard edges multiples of 384),
+ *     10 = 96 columns x 128 rows, 11 = 96 columns x 256 rows (clusters of four
+ *         as in 9; n and shard edges multiples of 384).
  * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
  * call (the conditions in parentheses).
  */
-#define EXL3_TEST_TILE_SHAPES 10
+#define EXL3_TEST_TILE_SHAPES 12
 exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
                                    const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                    const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,

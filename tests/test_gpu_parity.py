@@ -224,6 +224,7 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
                 assert bool((acc == 0).all()), f"shape {shape} m={m}: workspace not re-zeroed"
     # the cases reach every shape that their sizes allow
     need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
+    need |= {10, 11} if all(w % 384 == 0 for w in widths) else set()
     if not split and (k // 128) % 2 == 0:
         need |= {0, 8} | ({9} if all(w % 384 == 0 for w in widths) else set())
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
