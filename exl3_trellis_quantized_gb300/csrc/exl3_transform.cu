@@ -9,10 +9,11 @@
 //
 // Four lanes own one (row, 128-block): lane q of the four holds elements
 // 32q..32q+31, so a warp covers eight blocks (2 KB of x) per pass with 16-byte
-// loads and stores.  Butterfly stages of stride 1..16 stay in registers; the
-// stride-32 and stride-64 stages exchange with lanes q^1 and q^2.  Each stage
-// computes (a, b) -> (a + b, a - b) on the same pairs as the plain definition,
-// so the order of fp32 adds is the fixed one.  x is read once and reused for
+// loads and stores.  Butterfly stages of stride 1..16 stay in registers; for
+// the stride-32 and stride-64 stages the warp regroups its blocks once through
+// shared memory so that each lane holds four elements 32 apart (rotate_store).
+// Each stage computes (a, b) -> (a + b, a - b) on the same pairs as the plain
+// definition, so the order of fp32 adds is the fixed one.  x is read once and reused for
 // every shard.  The kernel is HBM/L2-bound: 2 bytes in, 2*S bytes out per
 // element.
 #include "exl3_device.cuh"
@@ -32,11 +33,17 @@ __device__ __forceinline__ void unpack8(const uint4 w, uint16_t (&e)[8]) {
   }
 }
 
-// The Hadamard butterfly of a lane's 32 values (stages of stride 1..16 in
-// registers, 32 and 64 with lanes q^1 and q^2), times 2^-4, rounded to fp16
+// The Hadamard butterfly of a lane's 32 values, times 2^-4, rounded to fp16
 // and stored at dst (nothing is stored when dst is null; the lane still takes
-// part in the exchanges).
-__device__ __forceinline__ void rotate_store(float (&v)[32], int q, uint16_t* dst) {
+// part in the exchange).  Stages of stride 1..16 run in registers.  For the
+// stride-32 and stride-64 stages the warp's eight blocks go through its
+// shared-memory area xp (8 x 128 floats) once: each lane then holds elements
+// j, j+32, j+64, j+96 for its eight j = 8q..8q+7 and finishes both stages in
+// registers.  Every stage still maps the same pairs (a, b) -> (a + b, a - b),
+// so the fp32 sums are the definition's, whoever computes them.  The 16-byte
+// chunks are stored with their slot XORed by (block & 1) | (quarter << 1), so
+// neither the writes nor the reads of a quarter-warp share a bank.
+__device__ __forceinline__ void rotate_store(float (&v)[32], int q, float* xp, uint16_t* dst) {
 #pragma unroll
   for (int st = 1; st < 32; st <<= 1) {
 #pragma unroll
@@ -48,26 +55,49 @@ __device__ __forceinline__ void rotate_store(float (&v)[32], int q, uint16_t* ds
       }
     }
   }
+  const int ul = (threadIdx.x & 31) >> 2;  // block of the warp's eight
+  float* blk = xp + ul * 128;
+  __syncwarp();  // the previous pass's reads of xp are done
 #pragma unroll
-  for (int st = 1; st <= 2; st <<= 1) {  // element strides 32 and 64
-    const bool upper = (q & st) != 0;
+  for (int i = 0; i < 8; ++i) {
+    const int slot = i ^ ((ul & 1) | (q << 1));
+    *reinterpret_cast<float4*>(blk + q * 32 + slot * 4) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+  __syncwarp();
+  float w[4][8];  // w[r][e] = element 32r + 8q + e
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float p = __shfl_xor_sync(0xffffffffu, v[i], st);
-      v[i] = upper ? (p - v[i]) : (v[i] + p);
+  for (int r = 0; r < 4; ++r) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int slot = (2 * q + h) ^ ((ul & 1) | (r << 1));
+      const float4 t = *reinterpret_cast<const float4*>(blk + r * 32 + slot * 4);
+      w[r][4 * h] = t.x;
+      w[r][4 * h + 1] = t.y;
+      w[r][4 * h + 2] = t.z;
+      w[r][4 * h + 3] = t.w;
     }
   }
-  if (dst != nullptr) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t w[4];
+  for (int e = 0; e < 8; ++e) {
+    const float b0 = w[0][e] + w[1][e], b1 = w[0][e] - w[1][e];  // stride 32
+    const float b2 = w[2][e] + w[3][e], b3 = w[2][e] - w[3][e];
+    w[0][e] = b0 + b2;  // stride 64
+    w[2][e] = b0 - b2;
+    w[1][e] = b1 + b3;
+    w[3][e] = b1 - b3;
+  }
+  if (dst != nullptr) {
+    uint16_t* base = dst - 32 * q;  // the block's first element
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t o[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint16_t lo = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i] * 0.0625f));  // 2^-4 exact
-        const uint16_t hi = __half_as_ushort(__float2half_rn(v[8 * c + 2 * i + 1] * 0.0625f));
-        w[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+        // 2^-4 is exact; both values rounded to fp16 by one conversion
+        const __half2 hv = __floats2half2_rn(w[r][2 * i] * 0.0625f, w[r][2 * i + 1] * 0.0625f);
+        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
       }
-      *reinterpret_cast<uint4*>(dst + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(base + 32 * r + 8 * q) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -79,6 +109,28 @@ __device__ __forceinline__ float to_f32(uint16_t e) {
   return X_BF16 ? __bfloat162float(__ushort_as_bfloat16(e)) : __half2float(__ushort_as_half(e));
 }
 
+// Both elements of a packed pair (low half first) as fp32, exactly: bf16 by
+// moving its bits to the top of the word, fp16 by the paired conversion.
+template <bool X_BF16>
+__device__ __forceinline__ float2 pair_to_f32(uint32_t w) {
+  if (X_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
+// v[0..7] = x * suh for one 16-byte chunk of each (exact in fp32).
+template <bool X_BF16>
+__device__ __forceinline__ void scale_chunk(const uint4 xw, const uint4 sw, float* v) {
+  const uint32_t xs[4] = {xw.x, xw.y, xw.z, xw.w};
+  const uint32_t ss[4] = {sw.x, sw.y, sw.z, sw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 xf = pair_to_f32<X_BF16>(xs[i]);
+    const float2 sf = pair_to_f32<false>(ss[i]);
+    v[2 * i] = xf.x * sf.x;
+    v[2 * i + 1] = xf.y * sf.y;
+  }
+}
+
 template <bool X_BF16>
 __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __restrict__ x, int64_t m, int64_t k,
                                                               const uint16_t* __restrict__ suh, int num_shards,
@@ -86,51 +138,52 @@ __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __
   // The GEMM that consumes xh may be scheduled now: it prefetches its weights
   // and waits for this grid to complete before it reads xh.
   pdl_launch_dependents();
+  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const int q = lane & 3;  // which 32 elements of the block
   const int64_t kb = k >> 7;
   const int64_t units = m * kb;
   const int64_t groups = (units + 7) / 8;  // eight blocks per warp and pass
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // element offset of this lane's 32 values in group g (or -1 past the end)
-  auto lane_offset = [&](int64_t g, int64_t* row) -> int64_t {
-    const int64_t u = g * 8 + (lane >> 2);
-    if (g >= groups || u >= units) return -1;
-    *row = u / kb;
-    return *row * k + (u - *row * kb) * 128 + 32 * q;
-  };
+  // The lane's unit u = g * 8 + lane / 4 advances by 8 * warps_total units a
+  // pass; its (row, block) is stepped, not divided out, each pass.
+  int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t step = 8 * warps_total;
+  const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
+  int64_t u = g * 8 + (lane >> 2);
+  int64_t row = u / kb, blk = u - row * kb;
   // x stays packed (bf16 / fp16 pairs) in registers; the next pass's words are
   // loaded before this pass computes, so two passes of loads are in flight
-  int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  int64_t row = 0;
-  int64_t off = lane_offset(g, &row);
   uint4 cur[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) cur[c] = off >= 0 ? *reinterpret_cast<const uint4*>(x + off + 8 * c) : make_uint4(0, 0, 0, 0);
-  for (; g < groups; g += warps_total) {
-    int64_t nrow = 0;
-    const int64_t noff = lane_offset(g + warps_total, &nrow);
+  for (int c = 0; c < 4; ++c)
+    cur[c] = (g < groups && u < units) ? *reinterpret_cast<const uint4*>(x + row * k + blk * 128 + 32 * q + 8 * c)
+                                       : make_uint4(0, 0, 0, 0);
+  for (; g < groups; g += warps_total, u += step) {
+    int64_t nrow = row + step_rows, nblk = blk + step_blk;
+    if (nblk >= kb) {
+      nblk -= kb;
+      nrow += 1;
+    }
+    const bool nok = g + warps_total < groups && u + step < units;
     uint4 nxt[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      nxt[c] = noff >= 0 ? *reinterpret_cast<const uint4*>(x + noff + 8 * c) : make_uint4(0, 0, 0, 0);
-    const int64_t col = off >= 0 ? off - row * k : 32 * q;
+      nxt[c] = nok ? *reinterpret_cast<const uint4*>(x + nrow * k + nblk * 128 + 32 * q + 8 * c) : make_uint4(0, 0, 0, 0);
+    const bool ok = u < units;
+    const int64_t col = ok ? blk * 128 + 32 * q : 32 * q;
     for (int s = 0; s < num_shards; ++s) {
       float v[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint16_t e[8], se[8];
-        unpack8(cur[c], e);
-        unpack8(*reinterpret_cast<const uint4*>(suh + (int64_t)s * k + col + 8 * c), se);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[8 * c + i] = to_f32<X_BF16>(e[i]) * __half2float(__ushort_as_half(se[i]));  // exact
-      }
-      rotate_store(v, q, off >= 0 ? xh + (int64_t)s * m * k + off : nullptr);
+      for (int c = 0; c < 4; ++c)
+        scale_chunk<X_BF16>(cur[c], *reinterpret_cast<const uint4*>(suh + (int64_t)s * k + col + 8 * c), v + 8 * c);
+      rotate_store(v, q, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
-    off = noff;
     row = nrow;
+    blk = nblk;
   }
 }
 
@@ -144,20 +197,17 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
                                                                      int64_t k, const uint16_t* __restrict__ suh,
                                                                      int num_shards, uint16_t* __restrict__ xh) {
   pdl_launch_dependents();
+  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const int q = lane & 3;
   const int64_t kb = k >> 7;
   const int64_t units = m * kb;
   const int64_t groups = (units + 7) / 8;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // (row, column) of this lane's 32 values in group g; false past the end
-  auto lane_pos = [&](int64_t g, int64_t* row, int64_t* col) -> bool {
-    const int64_t u = g * 8 + (lane >> 2);
-    if (g >= groups || u >= units) return false;
-    *row = u / kb;
-    *col = (u - *row * kb) * 128 + 32 * q;
-    return true;
-  };
+  // the lane's unit advances by 8 * warps_total a pass: (row, block) stepped
+  const int64_t step = 8 * warps_total;
+  const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
   auto load = [&](bool ok, int64_t row, int64_t col, uint4 (&gw)[4], uint4 (&uw)[4]) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -166,13 +216,20 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
     }
   };
   int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  int64_t row = 0, col = 0;
-  bool ok = lane_pos(g, &row, &col);
+  int64_t u = g * 8 + (lane >> 2);
+  int64_t row = u / kb, blk = u - row * kb;
+  bool ok = g < groups && u < units;
+  int64_t col = blk * 128 + 32 * q;
   uint4 cg[4], cu[4];
   load(ok, row, col, cg, cu);
-  for (; g < groups; g += warps_total) {
-    int64_t nrow = 0, ncol = 0;
-    const bool nok = lane_pos(g + warps_total, &nrow, &ncol);
+  for (; g < groups; g += warps_total, u += step) {
+    int64_t nrow = row + step_rows, nblk = blk + step_blk;
+    if (nblk >= kb) {
+      nblk -= kb;
+      nrow += 1;
+    }
+    const int64_t ncol = nblk * 128 + 32 * q;
+    const bool nok = g + warps_total < groups && u + step < units;
     uint4 ng[4], nu[4];
     load(nok, nrow, ncol, ng, nu);
     float h[32];
@@ -197,7 +254,7 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[8 * c + i] = h[8 * c + i] * __half2float(__ushort_as_half(se[i]));
       }
-      rotate_store(v, q, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
+      rotate_store(v, q, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
     }
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -206,6 +263,7 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
     }
     ok = nok;
     row = nrow;
+    blk = nblk;
     col = ncol;
   }
 }
@@ -223,6 +281,8 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
     int64_t rows, int32_t topk, const int32_t* __restrict__ block_expert, int32_t block,
     const uint16_t* __restrict__ suh, int num_shards, int num_experts, uint16_t* __restrict__ xh) {
   pdl_launch_dependents();
+  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
   const int q = lane & 3;
   const int64_t kb = k >> 7;
@@ -230,15 +290,28 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
   const int64_t groups = (units + 7) / 8;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t pairs = num_tokens * topk;
-  for (int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); g < groups; g += warps_total) {
-    const int64_t u = g * 8 + (lane >> 2);
+  const int block_shift = block == 32 ? 5 : 7;  // block is 32 or 128 rows
+  // the lane's unit advances by 8 * warps_total a pass: (row, block) stepped
+  const int64_t step = 8 * warps_total;
+  const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
+  int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  int64_t u = g * 8 + (lane >> 2);
+  int64_t ur = u / kb, ub = u - ur * kb;
+  for (; g < groups; g += warps_total, u += step) {
     const bool in_range = u < units;
-    const int64_t r = in_range ? u / kb : 0;
-    const int64_t col = (in_range ? (u - r * kb) * 128 : 0) + 32 * q;
-    const int e = in_range ? block_expert[r / block] : -1;
+    const int64_t r = in_range ? ur : 0;
+    const int64_t col = (in_range ? ub * 128 : 0) + 32 * q;
+    ub += step_blk;
+    ur += step_rows;
+    if (ub >= kb) {
+      ub -= kb;
+      ur += 1;
+    }
+    const int e = in_range ? block_expert[r >> block_shift] : -1;
     const bool live = e >= 0 && e < num_experts;
     const int64_t id = live ? (int64_t)sorted_ids[r] : -1;
-    const int64_t tok = (id >= 0 && id < pairs) ? id / topk : -1;
+    // pair ids stay below num_tokens * topk <= 2^28: a 32-bit division
+    const int64_t tok = (id >= 0 && id < pairs) ? (int64_t)((uint32_t)id / (uint32_t)topk) : -1;
     uint4 xw[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -246,17 +319,12 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
     for (int s = 0; s < num_shards; ++s) {
       float v[32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint16_t xe[8], se[8];
-        unpack8(xw[c], xe);
-        unpack8(tok >= 0 ? *reinterpret_cast<const uint4*>(suh + ((int64_t)e * num_shards + s) * k + col + 8 * c)
-                         : make_uint4(0, 0, 0, 0),
-                se);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          v[8 * c + i] = to_f32<X_BF16>(xe[i]) * __half2float(__ushort_as_half(se[i]));  // exact; 0 on padding
-      }
-      rotate_store(v, q, live ? xh + ((int64_t)s * rows + r) * k + col : nullptr);
+      for (int c = 0; c < 4; ++c)  // 0 on padding rows
+        scale_chunk<X_BF16>(xw[c],
+                            tok >= 0 ? *reinterpret_cast<const uint4*>(suh + ((int64_t)e * num_shards + s) * k + col + 8 * c)
+                                     : make_uint4(0, 0, 0, 0),
+                            v + 8 * c);
+      rotate_store(v, q, xp, live ? xh + ((int64_t)s * rows + r) * k + col : nullptr);
     }
   }
 }
