@@ -623,20 +623,21 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
   }
 }
 
-// Grouped GEMM: 32-row blocks on the small-batch tile, 128-row blocks on the
-// 128-row tile (both 128 columns, two k atoms per stage).
+// Grouped GEMM tiles (all 128 columns): 32-row blocks on the small-batch tile
+// with two or four k atoms per stage, 128-row blocks on the 128-row tile.
 template <int BITS, int CB>
-cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int block, cudaStream_t stream) {
-  if (block == 32) return launch_tc_variant<BITS, CB, 128, 1, 2, 32, 1, true>(maps, p, stream);
+cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int tile, cudaStream_t stream) {
+  if (tile == kMoeTile32) return launch_tc_variant<BITS, CB, 128, 1, 2, 32, 1, true>(maps, p, stream);
+  if (tile == kMoeTile32K4) return launch_tc_variant<BITS, CB, 128, 1, 4, 32, 1, true>(maps, p, stream);
   return launch_tc_variant<BITS, CB, 128, 1, 2, 128, 1, true>(maps, p, stream);
 }
 
 template <int BITS>
-cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int block, cudaStream_t stream) {
+cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int tile, cudaStream_t stream) {
   switch (cb) {
-    case CB_3INST: return launch_moe_cb<BITS, CB_3INST>(maps, p, block, stream);
-    case CB_MCG: return launch_moe_cb<BITS, CB_MCG>(maps, p, block, stream);
-    default: return launch_moe_cb<BITS, CB_MUL1>(maps, p, block, stream);
+    case CB_3INST: return launch_moe_cb<BITS, CB_3INST>(maps, p, tile, stream);
+    case CB_MCG: return launch_moe_cb<BITS, CB_MCG>(maps, p, tile, stream);
+    default: return launch_moe_cb<BITS, CB_MUL1>(maps, p, tile, stream);
   }
 }
 

@@ -472,21 +472,24 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
 cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  p.box_rows = block;  // both grouped tiles take two k atoms per stage: every row of the block
+  p.box_rows = block;  // every grouped tile holds several k atoms per stage: every row of the block
+  // 32-row blocks take four k atoms per stage when k holds an even number of 128-blocks
+  const int tile = block == 32 ? ((a.k / 128) % 2 == 0 ? kMoeTile32K4 : kMoeTile32) : kMoeTile128;
+  const int ka = tile == kMoeTile32K4 ? 4 : 2;
   TcMaps maps;
-  cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, 2);
+  cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, ka);
   if (e != cudaSuccess) return e;
-  e = make_moe_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, 128, 8, a.num_experts);
+  e = make_moe_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, 128, 4 * ka, a.num_experts);
   if (e != cudaSuccess) return e;
   switch (bits) {
-    case 1: return launch_moe_gemm_tc_bits<1>(maps, p, cb, block, stream);
-    case 2: return launch_moe_gemm_tc_bits<2>(maps, p, cb, block, stream);
-    case 3: return launch_moe_gemm_tc_bits<3>(maps, p, cb, block, stream);
-    case 4: return launch_moe_gemm_tc_bits<4>(maps, p, cb, block, stream);
-    case 5: return launch_moe_gemm_tc_bits<5>(maps, p, cb, block, stream);
-    case 6: return launch_moe_gemm_tc_bits<6>(maps, p, cb, block, stream);
-    case 7: return launch_moe_gemm_tc_bits<7>(maps, p, cb, block, stream);
-    default: return launch_moe_gemm_tc_bits<8>(maps, p, cb, block, stream);
+    case 1: return launch_moe_gemm_tc_bits<1>(maps, p, cb, tile, stream);
+    case 2: return launch_moe_gemm_tc_bits<2>(maps, p, cb, tile, stream);
+    case 3: return launch_moe_gemm_tc_bits<3>(maps, p, cb, tile, stream);
+    case 4: return launch_moe_gemm_tc_bits<4>(maps, p, cb, tile, stream);
+    case 5: return launch_moe_gemm_tc_bits<5>(maps, p, cb, tile, stream);
+    case 6: return launch_moe_gemm_tc_bits<6>(maps, p, cb, tile, stream);
+    case 7: return launch_moe_gemm_tc_bits<7>(maps, p, cb, tile, stream);
+    default: return launch_moe_gemm_tc_bits<8>(maps, p, cb, tile, stream);
   }
 }
 
