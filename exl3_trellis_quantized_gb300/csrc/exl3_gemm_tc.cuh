@@ -123,7 +123,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int CLX = C::kClusterX;
   constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
   const GemmArgs& a = p.a;
-  static_assert(!MOE || (RG == 1 && PAIR == 1 && BN == 128), "grouped GEMM: one row group of one CTA per block");
+  static_assert(!MOE || (RG == 1 && PAIR == 1 && (BN == 128 || BN == 96)),
+                "grouped GEMM: one row group per block, 128 columns or 96-column strips");
   // grouped GEMM: a block of no expert (-1, or an id past the last expert) is
   // skipped; the whole CTA leaves before it touches anything
   int expert = 0;
@@ -623,12 +624,14 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
   }
 }
 
-// Grouped GEMM tiles (all 128 columns): 32-row blocks on the small-batch tile
-// with two or four k atoms per stage, 128-row blocks on the 128-row tile.
+// Grouped GEMM tiles: 32-row blocks on the small-batch tile (128 columns with
+// two or four k atoms per stage, or 96-column strips in clusters of four),
+// 128-row blocks on the 128-row tile.
 template <int BITS, int CB>
 cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int tile, cudaStream_t stream) {
   if (tile == kMoeTile32) return launch_tc_variant<BITS, CB, 128, 1, 2, 32, 1, true>(maps, p, stream);
   if (tile == kMoeTile32K4) return launch_tc_variant<BITS, CB, 128, 1, 4, 32, 1, true>(maps, p, stream);
+  if (tile == kMoeTile32K4N96) return launch_tc_variant<BITS, CB, 96, 1, 4, 32, 1, true>(maps, p, stream);
   return launch_tc_variant<BITS, CB, 128, 1, 2, 128, 1, true>(maps, p, stream);
 }
 

@@ -117,8 +117,9 @@ int64_t tc_autotune_entries();
 template <int BITS>
 cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, TcShape shape,
                                 cudaStream_t stream);
-// Grouped GEMM tiles: 32-row blocks with two or four k atoms per stage, 128-row blocks.
-enum MoeTile : int { kMoeTile32 = 0, kMoeTile32K4 = 1, kMoeTile128 = 2 };
+// Grouped GEMM tiles: 32-row blocks with two or four k atoms per stage (or in
+// 96-column strips with four), 128-row blocks.
+enum MoeTile : int { kMoeTile32 = 0, kMoeTile32K4 = 1, kMoeTile128 = 2, kMoeTile32K4N96 = 3 };
 template <int BITS>
 cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int tile, cudaStream_t stream);
 // Read and clear the wait-timeout flags of every kernel translation unit (synchronous).

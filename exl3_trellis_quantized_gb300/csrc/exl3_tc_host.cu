@@ -473,13 +473,21 @@ cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, c
   TcParams p;
   p.a = a;
   p.box_rows = block;  // every grouped tile holds several k atoms per stage: every row of the block
-  // 32-row blocks take four k atoms per stage when k holds an even number of 128-blocks
-  const int tile = block == 32 ? ((a.k / 128) % 2 == 0 ? kMoeTile32K4 : kMoeTile32) : kMoeTile128;
-  const int ka = tile == kMoeTile32K4 ? 4 : 2;
+  // 32-row blocks take four k atoms per stage when k holds an even number of
+  // 128-blocks, and 96-column strips when the grid of every row block (live
+  // or not: the routing stays on the device) keeps more decode busy that way
+  int tile = block == 32 ? ((a.k / 128) % 2 == 0 ? kMoeTile32K4 : kMoeTile32) : kMoeTile128;
+  if (tile == kMoeTile32K4 && edges_multiple_of(a, 384)) {
+    const int64_t blocks = a.m / block;
+    if (small_batch_rate(blocks * (a.n / 96), kRel96) > small_batch_rate(blocks * (a.n / 128), 1.0))
+      tile = kMoeTile32K4N96;
+  }
+  const int ka = (tile == kMoeTile32K4 || tile == kMoeTile32K4N96) ? 4 : 2;
+  const int bn = tile == kMoeTile32K4N96 ? 96 : 128;
   TcMaps maps;
   cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, ka);
   if (e != cudaSuccess) return e;
-  e = make_moe_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, 128, 4 * ka, a.num_experts);
+  e = make_moe_trellis_map(&maps.trellis, a.trellis, a.k, a.n, bits, bn, 4 * ka, a.num_experts);
   if (e != cudaSuccess) return e;
   switch (bits) {
     case 1: return launch_moe_gemm_tc_bits<1>(maps, p, cb, tile, stream);

@@ -27,6 +27,7 @@ CASES = [
     (70, 4, 2, 128, 256, [384], 6, 0),
     (300, 16, 4, 128, 384, [128, 128], 5, 1),
     (9, 5, 2, 32, 384, [256], 2, 0),  # odd k/128: 32-row blocks on two k atoms per stage
+    (3, 6, 2, 32, 512, [384, 384], 4, 1),  # few blocks, 384-aligned shards: 96-column strips
 ]
 
 
