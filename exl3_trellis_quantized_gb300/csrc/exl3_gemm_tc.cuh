@@ -429,6 +429,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // block / cluster barriers below.
   const int dw = warp - kTcFirstDecoder;
   bool ok = true;
+  // The output scales of this lane's columns (pass 2 below), loaded before
+  // the wait for the accumulators so that their latency hides behind the
+  // last MMAs instead of stalling the epilogue.
+  constexpr int kSpanBlocks = C::kClusterX * BN / 128;
+  const uint32_t rank = (C::kClusterX > 1) ? cluster_ctarank() : 0u;
+  const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
+  float svf[kSpanBlocks][4];
+  if (warp >= kTcFirstDecoder && a.parts == 1) {
+#pragma unroll
+    for (int hb = 0; hb < kSpanBlocks; ++hb)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) svf[hb][i] = __half2float(__ushort_as_half(svh[cbase + hb * 128 + lane + 32 * i]));
+  }
   if (warp >= kTcFirstDecoder) {
     ok = mbar_wait(accfull, 0) && *failed == 0u;
     if (PAIR > 1) {
@@ -475,8 +488,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else {
-    const uint32_t rank = (CLX > 1) ? cluster_ctarank() : 0u;
-    const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
     constexpr int kSpan = CLX * BN;  // whole 128-column blocks
     for (int r = 0; r < RG; ++r) {
       // 1. tensor memory -> zs[128][BN].  Each thread holds one row's 32
@@ -508,8 +519,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // block of the span: the stride-32 and stride-64 stages, then scale and
       // store (each store instruction writes 32 consecutive columns)
       if (warp >= kTcFirstDecoder) {
+#pragma unroll
         for (int hb = 0; hb < kSpan / 128; ++hb) {
-          float svf[4];
           uint32_t zsrc[4];
           int64_t col[4];
 #pragma unroll
@@ -518,7 +529,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t src_rank = (uint32_t)(span_col / BN);
             const int local_col = span_col - (int)src_rank * BN;
             col[i] = cbase + span_col;
-            svf[i] = __half2float(__ushort_as_half(svh[col[i]]));
             zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
           }
           for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
@@ -538,7 +548,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             v[3] = a1 - a3;
             uint16_t* yr = y + row * a.n;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[i], bf16);
+            for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[hb][i], bf16);
           }
         }
       }
