@@ -435,12 +435,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int kSpanBlocks = C::kClusterX * BN / 128;
   const uint32_t rank = (C::kClusterX > 1) ? cluster_ctarank() : 0u;
   const int64_t cbase = c0 - (int64_t)rank * BN;  // first column of the cluster's span
-  float svf[kSpanBlocks][4];
+  // Without a cluster, pass 2 gives lane j = lane & 7 columns 4j..4j+3 of
+  // each 32-column quarter (four adjacent outputs per store); across a
+  // cluster's partner tiles it keeps one column per lane and quarter (scalar
+  // distributed-shared-memory loads measured faster there).
+  constexpr bool kPackedRows = C::kClusterX == 1;
+  float svf[kSpanBlocks][4];  // one column per lane and quarter
+  uint2 svw[kSpanBlocks][4];  // four adjacent columns per lane and quarter, fp16 packed
   if (warp >= kTcFirstDecoder && a.parts == 1) {
 #pragma unroll
     for (int hb = 0; hb < kSpanBlocks; ++hb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) svf[hb][i] = __half2float(__ushort_as_half(svh[cbase + hb * 128 + lane + 32 * i]));
+      for (int i = 0; i < 4; ++i) {
+        if constexpr (kPackedRows) {
+          svw[hb][i] = *reinterpret_cast<const uint2*>(svh + cbase + hb * 128 + 32 * i + 4 * (lane & 7));
+        } else {
+          svf[hb][i] = __half2float(__ushort_as_half(svh[cbase + hb * 128 + lane + 32 * i]));
+        }
+      }
   }
   if (warp >= kTcFirstDecoder) {
     ok = mbar_wait(accfull, 0) && *failed == 0u;
@@ -515,40 +527,105 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       } else {
         __syncthreads();
       }
-      // 2. rows: lane l owns columns l, l+32, l+64, l+96 of each 128-column
-      // block of the span: the stride-32 and stride-64 stages, then scale and
-      // store (each store instruction writes 32 consecutive columns)
-      if (warp >= kTcFirstDecoder) {
-#pragma unroll
-        for (int hb = 0; hb < kSpan / 128; ++hb) {
-          uint32_t zsrc[4];
-          int64_t col[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int span_col = hb * 128 + lane + 32 * i;
-            const uint32_t src_rank = (uint32_t)(span_col / BN);
-            const int local_col = span_col - (int)src_rank * BN;
-            col[i] = cbase + span_col;
-            zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
-          }
-          for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
-            const int64_t row = row0 + r * 128 + rr;
-            if (!ok || row >= row_end) break;  // rows ascend with rr
-            float v[4];
-#pragma unroll
+      if constexpr (kPackedRows) {
+        // 2. rows: eight lanes per row, four rows per warp step.  Lane j of a
+        // row owns columns 4j..4j+3 of each 32-column quarter of a 128-column
+        // block of the span: the stride-32 and stride-64 stages, then scale and
+        // store four adjacent outputs (8 bytes) per quarter.
+        if (warp >= kTcFirstDecoder) {
+          const int j = lane & 7, sr = lane >> 3;
+  #pragma unroll
+          for (int hb = 0; hb < kSpan / 128; ++hb) {
+            uint32_t zsrc[4];
+            int64_t col[4];
+            float sv[4][4];
+  #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
-              v[i] = (CLX > 1) ? ld_shared_cluster_f32(addr) : ld_shared_f32(addr);
+              // a quarter never straddles two CTAs: BN is a multiple of 32
+              const int span_col = hb * 128 + 32 * i + 4 * j;
+              const uint32_t src_rank = (uint32_t)(span_col / BN);
+              const int local_col = span_col - (int)src_rank * BN;
+              col[i] = cbase + span_col;
+              zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
+              const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].x));
+              const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].y));
+              sv[i][0] = s01.x;
+              sv[i][1] = s01.y;
+              sv[i][2] = s23.x;
+              sv[i][3] = s23.y;
             }
-            // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
-            const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-            v[0] = a0 + a2;
-            v[2] = a0 - a2;
-            v[1] = a1 + a3;
-            v[3] = a1 - a3;
-            uint16_t* yr = y + row * a.n;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[hb][i], bf16);
+            for (int rb = (int)rank + CLX * 4 * dw; rb < 128; rb += CLX * 4 * kTcDecodeWarps) {
+              const int rr = rb + CLX * sr;  // < 128: rb + 3 * CLX stays inside the group
+              const int64_t row = row0 + r * 128 + rr;
+              float v[4][4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
+                const float4 t = (CLX > 1) ? ld_shared_cluster_v4f(addr) : ld_shared_v4f(addr);
+                v[i][0] = t.x;
+                v[i][1] = t.y;
+                v[i][2] = t.z;
+                v[i][3] = t.w;
+              }
+              if (ok && row < row_end) {
+                uint16_t* yr = y + row * a.n;
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
+                  const float a0 = v[0][e] + v[1][e], a1 = v[0][e] - v[1][e];
+                  const float a2 = v[2][e] + v[3][e], a3 = v[2][e] - v[3][e];
+                  v[0][e] = a0 + a2;
+                  v[2][e] = a0 - a2;
+                  v[1][e] = a1 + a3;
+                  v[3][e] = a1 - a3;
+                }
+  #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t o[4];
+  #pragma unroll
+                  for (int e = 0; e < 4; ++e) o[e] = f32_to_out((v[i][e] * 0.125f) * sv[i][e], bf16);
+                  *reinterpret_cast<uint2*>(yr + col[i]) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+                }
+              }
+            }
+          }
+        }
+      } else {
+        // 2. rows: lane l owns columns l, l+32, l+64, l+96 of each 128-column
+        // block of the span: the stride-32 and stride-64 stages, then scale and
+        // store (each store instruction writes 32 consecutive columns)
+        if (warp >= kTcFirstDecoder) {
+  #pragma unroll
+          for (int hb = 0; hb < kSpan / 128; ++hb) {
+            uint32_t zsrc[4];
+            int64_t col[4];
+  #pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int span_col = hb * 128 + lane + 32 * i;
+              const uint32_t src_rank = (uint32_t)(span_col / BN);
+              const int local_col = span_col - (int)src_rank * BN;
+              col[i] = cbase + span_col;
+              zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
+            }
+            for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
+              const int64_t row = row0 + r * 128 + rr;
+              if (!ok || row >= row_end) break;  // rows ascend with rr
+              float v[4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
+                v[i] = (CLX > 1) ? ld_shared_cluster_f32(addr) : ld_shared_f32(addr);
+              }
+              // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
+              const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+              v[0] = a0 + a2;
+              v[2] = a0 - a2;
+              v[1] = a1 + a3;
+              v[3] = a1 - a3;
+              uint16_t* yr = y + row * a.n;
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[hb][i], bf16);
+            }
           }
         }
       }
