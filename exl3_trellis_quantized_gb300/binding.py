@@ -62,6 +62,9 @@ def lib() -> ctypes.CDLL:
     L.exl3_test_gemm_shape.restype = ctypes.c_int
     L.exl3_test_codebook.argtypes = [ctypes.c_int, vp, vp]
     L.exl3_test_unpack.argtypes = [vp, i32, ctypes.c_int, i64, i64, vp, vp]
+    L.exl3_test_tile_plan.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_int32), i32, i32,
+                                      ctypes.POINTER(ctypes.c_int64)]
+    L.exl3_test_tile_plan.restype = ctypes.c_int
     L.exl3_set_autotune.argtypes = [i32]
     L.exl3_set_autotune.restype = ctypes.c_int
     L.exl3_clear_autotune.argtypes = []
@@ -85,6 +88,14 @@ def device_status() -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().exl3_device_status(ctypes.byref(flags)), "exl3_device_status")
     return int(flags.value)
+
+
+def test_tile_plan(m: int, k: int, n: int, shard_cols: Sequence[int], split: bool = False) -> tuple:
+    """The cost model's plan (host only): (shape, tail shape or -1, pair tiles, tail row, tail column)."""
+    cols, ns = _cols(shard_cols)
+    out = (ctypes.c_int64 * 5)()
+    _check(lib().exl3_test_tile_plan(m, k, n, cols, ns, 1 if split else 0, out), "exl3_test_tile_plan")
+    return tuple(int(v) for v in out)
 
 
 def set_autotune(enable: bool) -> None:

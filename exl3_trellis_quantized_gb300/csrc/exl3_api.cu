@@ -222,6 +222,23 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
                      "exl3_test_unpack");
 }
 
+exl3_status_t exl3_test_tile_plan(int64_t m, int64_t k, int64_t n, const int32_t* shard_cols, int32_t num_shards,
+                                  int32_t split, int64_t* out) {
+  if (m < 1 || m > kMaxRows || !valid_kn(k) || !valid_kn(n) || out == nullptr) return EXL3_EINVAL;
+  if (num_shards < 1 || num_shards > EXL3_MAX_SHARDS || !valid_shards(shard_cols, num_shards, n)) return EXL3_EINVAL;
+  if (split != 0 && split != 1) return EXL3_EINVAL;
+  exl3::GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.m = m;
+  a.k = k;
+  a.n = n;
+  a.num_shards = num_shards;
+  for (int i = 0; i <= num_shards; ++i) a.shard_cols[i] = shard_cols[i];
+  a.parts = split ? exl3_splitk_parts(k, n) : 1;
+  exl3::tc_plan(a, out);
+  return EXL3_OK;
+}
+
 exl3_status_t exl3_set_autotune(int32_t enable) {
   if (enable != 0 && enable != 1) return EXL3_EINVAL;
   exl3::tc_set_autotune(enable == 1);

@@ -108,6 +108,11 @@ enum class TcShape : int {
 // shape < 0: chosen from the sizes; otherwise a TcShape value that
 // tc_shape_supported() accepted.
 cudaError_t launch_gemm_tc(const GemmArgs& args, int bits, int cb, cudaStream_t stream, int shape = -1);
+// The cost model's plan for a call (host only, no launch): out[0] the tile
+// shape; for a pair shape whose last wave is split off, out[1] the second
+// launch's shape, out[2] the pair tiles of the first, out[3] / out[4] the
+// first row / column of the second; else out[1] = -1.
+void tc_plan(const GemmArgs& args, int64_t out[5]);
 // Whether tile shape `shape` can run the call described by `args`.
 bool tc_shape_supported(int shape, const GemmArgs& args);
 // Tile-shape autotune (see exl3_tc_host.cu): switch, cache reset, cache size.

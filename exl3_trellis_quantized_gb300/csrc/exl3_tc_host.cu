@@ -284,6 +284,22 @@ TcShape choose_shape(const GemmArgs& a) {
 
 }  // namespace
 
+void tc_plan(const GemmArgs& a, int64_t out[5]) {
+  const TcShape s = choose_shape(a);
+  out[0] = (int64_t)s;
+  out[1] = -1;
+  out[2] = out[3] = out[4] = 0;
+  if (dims_of(s).pair > 1) {
+    const TailPlan t = plan_tail(a, s);
+    if (t.split) {
+      out[1] = (int64_t)t.tail;
+      out[2] = t.primary_tiles;
+      out[3] = t.row_base;
+      out[4] = t.col_base;
+    }
+  }
+}
+
 bool tc_shape_supported(int shape, const GemmArgs& a) {
   if (shape < 0 || shape > (int)TcShape::kLast) return false;
   const TcShape s = (TcShape)shape;

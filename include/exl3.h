@@ -269,6 +269,20 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
                                    void* stream);
 
 /*
+ * exl3_test_tile_plan: the cost model's plan for an exl3_gemm call (split = 0)
+ * or exl3_gemm_splitk call (split = 1) of the given sizes, computed on the host
+ * with no launch (the SM count of the current device, 152 when there is none).
+ * out[0] = tile shape (numbered as in exl3_test_gemm_shape); for a pair shape
+ * whose partial last wave runs as a second launch of smaller tiles, out[1] =
+ * that launch's shape, out[2] = pair tiles of the first launch, out[3] and
+ * out[4] = first row and first column of the second launch; otherwise
+ * out[1] = -1 and out[2..4] = 0.  EXL3_EINVAL for invalid sizes or shard map.
+ * No counterpart in the pages: the tiling is this library's own.
+ */
+exl3_status_t exl3_test_tile_plan(int64_t m, int64_t k, int64_t n, const int32_t* shard_cols, int32_t num_shards,
+                                  int32_t split, int64_t* out);
+
+/*
  * Tile-shape autotune (off by default).  The best tile for a batch size
  * depends on the layer's shape too, so the shape is timed once per distinct
  * shape and cached, never while a CUDA graph is being captured, and the cost

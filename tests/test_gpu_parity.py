@@ -320,6 +320,7 @@ SPLIT_CASES = [
     (256, [12288], 4, 1, 1024),  # 192 pair CTAs: 40 of them become 256-row x 128-column tiles
     (256, [10240, 2048], 3, 0, 1024),  # the split-off columns span both shards
     (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 128 x 128 tiles
+    (256, [7680], 4, 1, 3000),  # a ragged last row pair (440 rows) in the split-off tiles
 ]
 
 

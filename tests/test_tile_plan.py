@@ -1,0 +1,60 @@
+"""The cost model's tile plan (host only, no GPU): pins of the decisions the
+GEMM's measured shape costs lead to on a 152-SM GB300, and the invariants of a
+split last wave (the first launch is whole waves; the second covers exactly the
+pair tiles left)."""
+import pytest
+
+from exl3_trellis_quantized_gb300 import binding as B
+
+SMS = 152  # the plan uses the current device's SM count, 152 without one
+N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2 = range(12)
+PAIR_BN = {N128R2P: 128, N256R2P: 256}
+
+
+def plan(m, k, n, cols=None, split=False):
+    return B.test_tile_plan(m, k, n, cols or [0, n], split)
+
+
+@pytest.mark.parametrize("m,want", [
+    (1, (N96SK4, -1, 0, 0, 0)), (16, (N96SK4, -1, 0, 0, 0)),  # 96 column blocks: 96-column strips, 128 SMs
+    (64, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
+    (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
+    (1024, (N256R2P, N128R2, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 80 256x128 tiles
+    (4096, (N256R2P, N128, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 32 128x128 tiles
+])
+def test_q_proj_plan(m, want):
+    assert plan(m, 5120, 12288) == want
+
+
+def test_narrow_and_split_layers():
+    assert plan(16, 12288, 4096)[0] == N32S  # 32 column blocks: 32-column strips on 128 SMs
+    assert plan(16, 5120, 34816, [0, 17408, 34816])[0] == N128SK4  # 272 blocks fill the GPU at 128 columns
+    assert plan(16, 384, 4096)[0] != N32S  # odd k/128: no four-atom tiles
+    # split-k down projection: 7 parts of 40 blocks; 256-column CTAs need fewer waves
+    assert plan(16, 17408, 5120, split=True)[0] == N256R2
+
+
+@pytest.mark.parametrize("m,k,n", [(1024, 5120, 12288), (4096, 5120, 12288), (2048, 5120, 34816),
+                                   (4096, 5120, 34816), (3000, 4096, 7680), (1500, 2048, 20480)])
+def test_split_last_wave_invariants(m, k, n):
+    shape, tail, primary, row_base, col_base = plan(m, k, n)
+    if shape not in PAIR_BN or tail < 0:
+        return
+    bn = PAIR_BN[shape]
+    rows_per_pair_tile = 512
+    ncol = n // bn
+    nrp = -(-m // rows_per_pair_tile)
+    total_tiles = ncol * nrp
+    assert (2 * primary) % SMS == 0, "the first launch is whole waves"
+    assert row_base == (nrp - 1) * rows_per_pair_tile, "the split-off tiles are in the last row pair"
+    assert (n - col_base) // bn == total_tiles - primary, "the second launch covers exactly the tiles left"
+    assert col_base % bn == 0 and tail in (N128, N128R2, N256R2)
+
+
+def test_plan_rejects_invalid():
+    with pytest.raises(B.Exl3Error):
+        B.test_tile_plan(0, 5120, 12288, [0, 12288])
+    with pytest.raises(B.Exl3Error):
+        B.test_tile_plan(16, 5000, 12288, [0, 12288])
+    with pytest.raises(B.Exl3Error):
+        B.test_tile_plan(16, 5120, 12288, [0, 100, 12288])
