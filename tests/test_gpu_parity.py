@@ -346,3 +346,21 @@ def test_split_last_wave_byte_equal(k, widths, bits, cb, m):
     ref = _oracle(x[rows], layer, blocks)
     got = _np(single)[rows].reshape(len(rows), n // 128, 128)[:, blocks].reshape(len(rows), -1)
     _assert_columns(got, ref)
+
+
+def test_max_batch_rows():
+    """The largest batch the library accepts (2^22 rows): sampled rows against
+    the oracle, and rows byte-equal to a small batch of the same inputs."""
+    m, k, bits, cb = 1 << 22, 128, 3, 1
+    layer = synthetic.make_layer(k, [256], bits, cb, seed=2200)
+    x = synthetic.make_x(m, k, seed=2201)
+    tr, suh, svh = _dev(layer)
+    y = E.gemm(E.input_transform(x.to(DEV), suh), tr, bits, cb, svh, layer.shard_cols)
+    torch.cuda.synchronize()
+    rows = np.r_[0:16, (m // 2):(m // 2 + 16), (m - 16):m]
+    ref = _oracle(x[rows], layer)
+    _assert_columns(_np(y)[rows], ref, "max rows")
+    small = E.gemm(E.input_transform(x[:300].to(DEV), suh), tr, bits, cb, svh, layer.shard_cols)
+    assert torch.equal(small.view(torch.int16), y[:300].view(torch.int16))
+    tail = E.gemm(E.input_transform(x[m - 40:].to(DEV), suh), tr, bits, cb, svh, layer.shard_cols)
+    assert torch.equal(tail.view(torch.int16), y[m - 40:].view(torch.int16))
