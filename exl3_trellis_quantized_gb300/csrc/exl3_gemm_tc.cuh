@@ -651,11 +651,15 @@ template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool M
 cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
   using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
   auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, MOE>;
-  static bool configured = false;  // benign race: every thread sets the same attribute
-  if (!configured) {
+  // the shared-memory opt-in, once per device (benign race: every thread sets
+  // the same attribute)
+  static bool configured[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!configured[dev]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   // a pair's second CTA may own only rows past m: it still decodes its half
