@@ -182,7 +182,13 @@ def run_gpu(args, wl_name):
     accs = [torch.zeros(max(1, E.splitk_workspace_bytes(m, k, n) // 4), dtype=torch.float32, device=dev)
             if split else None for m in ms]
     stream = torch.cuda.current_stream(dev)
-    launches_per_linear = 2 + (1 if split and E.splitk_parts(k, n) > 1 else 0)
+    # launches per step: per batch size the transform, the GEMM (two launches
+    # when the cost model splits off a pair tile's last wave) and, under
+    # split-k, the epilogue
+    from exl3_trellis_quantized_gb300 import binding as EB
+    launches_per_step = sum(
+        2 + (1 if EB.test_tile_plan(m, k, n, layer.shard_cols, split)[1] >= 0 else 0)
+        + (1 if split and E.splitk_parts(k, n) > 1 else 0) for m in ms)
 
     def one_linear(i, it):
         tr = trs[it % copies]
@@ -418,7 +424,7 @@ def run_gpu(args, wl_name):
                        "l2": f"weights rotate over {copies} copies ({copies * wbytes / 1e6:.0f} MB > 3x L2)"},
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": launches_per_linear * len(ms) * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline,
             "sweep": sweep,
             "clocks": clk,
@@ -570,6 +576,7 @@ def run_mlp(args):
     import torch
 
     import exl3_trellis_quantized_gb300 as E
+    from exl3_trellis_quantized_gb300 import binding as EB
     from exl3_trellis_quantized_gb300 import synthetic
 
     dev = torch.device("cuda", 0)
@@ -641,7 +648,10 @@ def run_mlp(args):
                                f"down {db}-bit mul1 split-k, m={ms}",
                    "l2": f"weights rotate over {copies} copies"},
         "unfused_swiglu_ms_per_step": round(t_unfused * 1e3, 4),
-        "gpu_launches": (4 + (1 if E.splitk_parts(inter, hid) > 1 else 0)) * len(ms) * args.steps,
+        "gpu_launches": sum(
+            4 + (1 if E.splitk_parts(inter, hid) > 1 else 0)
+            + (1 if EB.test_tile_plan(m, hid, 2 * inter, gu.shard_cols, False)[1] >= 0 else 0)
+            + (1 if EB.test_tile_plan(m, inter, hid, dn.shard_cols, True)[1] >= 0 else 0) for m in ms) * args.steps,
         "clocks": clk, "peaks": {**peaks, "source": peak_src},
     }
 
