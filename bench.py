@@ -683,7 +683,9 @@ def run_moe(args):
     suh, svh = layer.suh.to(dev), layer.svh.to(dev)
     runs = []
     for t in MOE["tokens"]:
-        block = 32 if t * topk < 32 * ne else 128  # few rows per expert: the small block
+        # few routed rows per expert: small blocks (16 at about one row per expert,
+        # the pages' floor; 32 below 32 rows per expert), else 128
+        block = 16 if t * topk <= ne else 32 if t * topk < 32 * ne else 128
         r = synthetic.make_routing(t, ne, topk, block, seed=1202 + t, empty_blocks=0)
         x = synthetic.make_x(t, hid, seed=1203).to(dev)
         ids, be = r.sorted_ids.to(dev), r.block_expert.to(dev)

@@ -41,6 +41,9 @@ bool valid_shards(const int32_t* cols, int32_t s, int64_t n) {
 }
 
 // Validates everything exl3_gemm and exl3_gemm_splitk share and fills `a`.
+// Grouped row blocks: 16 (the pages' floor for few tokens per expert), 32 or 128 rows.
+bool valid_moe_block(int32_t block) { return block == 16 || block == 32 || block == 128; }
+
 exl3_status_t check_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
                          exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
                          void* y, exl3_dtype_t y_dtype, int64_t n, exl3::GemmArgs* a) {
@@ -100,7 +103,7 @@ exl3_status_t exl3_moe_input_transform(const void* x, exl3_dtype_t x_dtype, int6
                                        const int32_t* block_expert, int32_t block, const uint16_t* suh,
                                        int32_t num_shards, int32_t num_experts, uint16_t* xh, void* stream) {
   if (num_tokens < 0 || num_tokens > kMaxRows || rows < 0 || rows > kMaxRows || !valid_kn(k)) return EXL3_EINVAL;
-  if (!valid_dtype(x_dtype) || topk < 1 || topk > 64 || (block != 32 && block != 128) || rows % block) {
+  if (!valid_dtype(x_dtype) || topk < 1 || topk > 64 || !valid_moe_block(block) || rows % block) {
     return EXL3_EINVAL;
   }
   if (num_shards < 1 || num_shards > EXL3_MAX_SHARDS || num_experts < 1) return EXL3_EINVAL;
@@ -121,13 +124,14 @@ exl3_status_t exl3_moe_gemm(const uint16_t* xh, int64_t rows, int64_t k, const i
   exl3::GemmArgs a;
   exl3_status_t st = check_gemm(xh, rows, k, trellis, bits, cb, svh, shard_cols, num_shards, y, y_dtype, n, &a);
   if (st != EXL3_OK) return st;
-  if ((block != 32 && block != 128) || rows % block || num_experts < 1) return EXL3_EINVAL;
+  if (!valid_moe_block(block) || rows % block || num_experts < 1) return EXL3_EINVAL;
   // the expert index times one expert's trellis bytes must fit the tensor map's strides
   if ((int64_t)num_experts * (k / 16) * (n / 16) * 32 * bits > (int64_t(1) << 40)) return EXL3_EINVAL;
   if (rows == 0) return EXL3_OK;
   if (block_expert == nullptr) return EXL3_EINVAL;
   a.block_expert = block_expert;
   a.num_experts = num_experts;
+  a.moe_block = block;
   return cuda_status(exl3::launch_moe_gemm_tc(a, bits, cb, block, static_cast<cudaStream_t>(stream)), "exl3_moe_gemm");
 }
 

@@ -110,9 +110,10 @@ struct TcCfg {
   static_assert((2 * kNT + 2 * kNX + 3 * kNW + 1) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
 
-// MOE: grouped GEMM over row blocks of XR rows (one row group), each with its
-// own expert: blockIdx.y is the block, a.block_expert[block] the expert (the
-// trellis map then has the experts as a fourth dimension and svh is [E][n]).
+// MOE: grouped GEMM over row blocks of a.moe_block rows (at most XR, one row
+// group), each with its own expert: blockIdx.y is the block,
+// a.block_expert[block] the expert (the trellis map then has the experts as a
+// fourth dimension and svh is [E][n]).
 template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool MOE = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     row0 = a.row_base + (rp * 2 + prank) * (128 * RG);
   } else {
     c0 = a.col_base + (int64_t)blockIdx.x * BN;
-    row0 = (MOE ? 0 : a.row_base) + (int64_t)blockIdx.y * (MOE ? XR : 128 * RG);
+    row0 = MOE ? (int64_t)blockIdx.y * a.moe_block : a.row_base + (int64_t)blockIdx.y * (128 * RG);
   }
   const int part = (int)blockIdx.z;
   // this CTA's k range in 64-wide atoms: whole 128-row blocks of k per part
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool bf16 = a.y_bf16 != 0;
   // rows this CTA stores: a grouped block owns exactly its XR rows (the rows
   // after it belong to other blocks); otherwise everything below m
-  const int64_t row_end = MOE ? row0 + XR : a.m;
+  const int64_t row_end = MOE ? row0 + a.moe_block : a.m;
   uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
   float* zs = reinterpret_cast<float*>(rings);
   constexpr int kZ = C::kZStride;
@@ -666,7 +667,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
   if (PAIR > 1) {
     cfg.gridDim = dim3((unsigned)(2 * p.a.pair_tiles), 1u, (unsigned)p.a.parts);
   } else {
-    const int64_t row_blocks = MOE ? p.a.m / XR : (p.a.m - p.a.row_base + 128 * RG - 1) / (128 * RG);
+    const int64_t row_blocks = MOE ? p.a.m / p.a.moe_block : (p.a.m - p.a.row_base + 128 * RG - 1) / (128 * RG);
     cfg.gridDim = dim3((unsigned)((p.a.n - p.a.col_base) / BN), (unsigned)row_blocks, (unsigned)p.a.parts);
   }
   cfg.blockDim = dim3(kTcThreads, 1, 1);

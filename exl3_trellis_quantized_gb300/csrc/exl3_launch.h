@@ -45,6 +45,7 @@ struct GemmArgs {
   int64_t row_base, col_base;
   int32_t tile_cols, pair_tiles;
   int32_t trigger_dependents;
+  int32_t moe_block;  // grouped GEMM: rows per block (16, 32 or 128)
 };
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,

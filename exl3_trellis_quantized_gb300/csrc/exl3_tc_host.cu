@@ -488,11 +488,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
 cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  p.box_rows = block;  // every grouped tile holds several k atoms per stage: every row of the block
+  // every grouped tile holds several k atoms per stage, so a copy brings every
+  // row of the tile's region (a 16-row block rides on the 32-row tile: its
+  // second 16 rows are the next block's or zero fill, computed and not stored)
+  p.box_rows = block == 128 ? 128 : 32;
   // 32-row blocks take four k atoms per stage when k holds an even number of
   // 128-blocks, and 96-column strips when the grid of every row block (live
   // or not: the routing stays on the device) keeps more decode busy that way
-  int tile = block == 32 ? ((a.k / 128) % 2 == 0 ? kMoeTile32K4 : kMoeTile32) : kMoeTile128;
+  int tile = block <= 32 ? ((a.k / 128) % 2 == 0 ? kMoeTile32K4 : kMoeTile32) : kMoeTile128;
   if (tile == kMoeTile32K4 && edges_multiple_of(a, 384)) {
     const int64_t blocks = a.m / block;
     if (small_batch_rate(blocks * (a.n / 96), kRel96) > small_batch_rate(blocks * (a.n / 128), 1.0))

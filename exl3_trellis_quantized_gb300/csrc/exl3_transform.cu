@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
   const int64_t groups = (units + 7) / 8;
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t pairs = num_tokens * topk;
-  const int block_shift = block == 32 ? 5 : 7;  // block is 32 or 128 rows
+  const int block_shift = block == 16 ? 4 : block == 32 ? 5 : 7;  // block is 16, 32 or 128 rows
   // the lane's unit advances by 8 * warps_total a pass: (row, block) stepped
   const int64_t step = 8 * warps_total;
   const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;

@@ -162,7 +162,9 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
  *   block_expert  device int32 [rows / block]: expert of each block; -1 (or an
  *                 id >= num_experts) marks a block of no expert, which both
  *                 calls skip (such blocks may sit between live ones)
- *   block         32 or 128; rows a multiple of block
+ *   block         16, 32 or 128; rows a multiple of block (16 is the pages'
+ *                 floor, used when few tokens reach each expert: cuda-exl3
+ *                 README, "MoE notes")
  *
  * exl3_moe_input_transform: since suh is per expert (and per shard), the input
  * rotation happens after routing: each padded row of a live block gets its
@@ -182,7 +184,7 @@ exl3_status_t exl3_gemm_splitk(const uint16_t* xh, int64_t m, int64_t k, const i
  *   y        device, [rows][n] of y_dtype (output, in padded-row order; the
  *            weighted combine over each token's top-k rows is the caller's)
  * Validation and empty input as for exl3_gemm; EXL3_EINVAL also for a block
- * size other than 32 or 128, rows not a multiple of it, or no experts.  The
+ * size other than 16, 32 or 128, rows not a multiple of it, or no experts.  The
  * kernel reads block_expert before it waits for the previous kernel in the
  * stream, like the trellis (see exl3_gemm).
  */

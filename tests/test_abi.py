@@ -126,6 +126,10 @@ def test_moe_entry_points_reject_invalid(L):
     assert L.exl3_moe_gemm(v, 40, 256, v, 4, 1, v, cols, 1, v, 32, 4, v, 1, 256, None) == 1
     assert L.exl3_moe_gemm(v, 64, 256, v, 4, 1, v, cols, 1, None, 32, 4, v, 1, 256, None) == 1  # no block ids
     assert L.exl3_moe_gemm(v, 0, 256, v, 4, 1, v, cols, 1, v, 32, 4, v, 1, 256, None) == 0
+    # 16-row blocks are accepted (empty batches, so nothing launches)
+    assert L.exl3_moe_input_transform(v, 1, 4, 256, v, 0, 2, v, 16, v, 1, 4, v, None) == 0
+    assert L.exl3_moe_gemm(v, 0, 256, v, 4, 1, v, cols, 1, v, 16, 4, v, 1, 256, None) == 0
+    assert L.exl3_moe_gemm(v, 24, 256, v, 4, 1, v, cols, 1, v, 16, 4, v, 1, 256, None) == 1  # 24 rows: not whole blocks
 
 
 def test_test_entry_points_reject_invalid(L):

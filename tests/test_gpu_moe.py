@@ -28,6 +28,8 @@ CASES = [
     (300, 16, 4, 128, 384, [128, 128], 5, 1),
     (9, 5, 2, 32, 384, [256], 2, 0),  # odd k/128: 32-row blocks on two k atoms per stage
     (3, 6, 2, 32, 512, [384, 384], 4, 1),  # few blocks, 384-aligned shards: 96-column strips
+    (4, 10, 2, 16, 256, [256], 4, 1),  # 16-row blocks (few tokens per expert)
+    (7, 5, 3, 16, 384, [128, 128], 3, 2),  # 16-row blocks, odd k/128
 ]
 
 
