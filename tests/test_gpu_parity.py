@@ -364,3 +364,19 @@ def test_max_batch_rows():
     assert torch.equal(small.view(torch.int16), y[:300].view(torch.int16))
     tail = E.gemm(E.input_transform(x[m - 40:].to(DEV), suh), tr, bits, cb, svh, layer.shard_cols)
     assert torch.equal(tail.view(torch.int16), y[m - 40:].view(torch.int16))
+
+
+@pytest.mark.parametrize("k,widths,bits,cb,split", [
+    (1024, [12288], 6, 1, False),  # 96-column strips alone, pairs in the batch
+    (512, [384, 384], 4, 2, False),
+    (2048, [512], 3, 0, True),
+])
+def test_each_row_alone_equals_its_row_in_a_batch(k, widths, bits, cb, split):
+    """Rows never mix: any row computed on its own has the bytes it has inside a
+    300-row batch (not only the batch's first rows)."""
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=2300 + k + bits)
+    x = synthetic.make_x(300, k, seed=2301)
+    y, _ = _run(layer, x, torch.bfloat16, split)
+    for r in (0, 17, 150, 299):
+        yr, _ = _run(layer, x[r:r + 1], torch.bfloat16, split)
+        assert torch.equal(yr.view(torch.int16), y[r:r + 1].view(torch.int16)), f"row {r} differs alone"
