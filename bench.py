@@ -126,6 +126,26 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(value, device):
+    """The largest value over the ranks of the process group (the slowest
+    replica's time), or the value itself without one; every rank gets it."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(sol_seconds_per_step, steps, world, elapsed):
+    """Whole-job % of the 1-GPU roofline: every replica runs `steps` steps of
+    the workload, so the job does world * steps of speed-of-light work in the
+    slowest replica's time."""
+    return 100.0 * sol_seconds_per_step * steps * world / elapsed
+
+
 def recorded_traffic(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -232,11 +252,7 @@ def run_gpu(args, wl_name):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    elapsed = t0.elapsed_time(t1) / 1e3
-    if world > 1:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dev)
 
     # per-batch-size breakdown, measured separately (same launches, events around each)
     reps = max(3, min(args.steps, 50))
@@ -293,7 +309,7 @@ def run_gpu(args, wl_name):
     del ruler_src, ruler_dst
 
     sol_step = sum(sol_seconds(m, k, n, bits, peaks)[0] for m in ms)
-    value = 100.0 * sol_step * args.steps * world / elapsed
+    value = replica_throughput(sol_step, args.steps, world, elapsed)
 
     # dominant GEMM launch: the batch size that takes the longest.  Each batch
     # size's GEMM runs `reps` times back to back between two events (weights
@@ -403,12 +419,8 @@ def run_gpu(args, wl_name):
     join_copies()
     e1.record(stream)
     torch.cuda.synchronize()
-    e_el = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e_el], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e_el = float(t.item())
-    e2e_value = 100.0 * sol_step * args.steps * world / e_el
+    e_el = max_over_ranks(e0.elapsed_time(e1) / 1e3, dev)
+    e2e_value = replica_throughput(sol_step, args.steps, world, e_el)
 
     out = None
     if rank == 0:
