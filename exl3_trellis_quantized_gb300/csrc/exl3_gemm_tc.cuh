@@ -8,10 +8,13 @@
 // spans whole 128-column Hadamard blocks (32 columns: 4 CTAs over one block;
 // 96 columns: 4 CTAs over three): each CTA accumulates its own columns and the
 // epilogue reads the partners' fp32 tiles through distributed shared memory,
-// so the arithmetic is the same whatever BN is.  With PAIR = 2 two CTAs that own the same columns and
-// neighbouring rows form a cluster: each decodes half of the columns and copies
-// its half of the decoded operand into the partner's shared memory, so every
-// decoded weight feeds 2*RG*128 rows.
+// so the arithmetic is the same whatever BN is.  With PAIR = 2 two CTAs that
+// own the same columns and neighbouring rows form a cluster {2, 1, 1}: each
+// decodes half of the columns and copies its half of the decoded operand into
+// the partner's shared memory, so every decoded weight feeds 2*RG*128 rows.
+// A pair launch may cover only whole waves of pair tiles (numbered row pair
+// major), the rest going to a second launch of smaller tiles (row_base /
+// col_base), see exl3_tc_host.cu.
 //
 // Shared memory holds three rings, each with its own depth: rotated
 // activations (NX slots, RG row groups of KA swizzle atoms of 64 k), decoded
