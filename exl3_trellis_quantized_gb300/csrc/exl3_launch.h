@@ -102,7 +102,9 @@ enum class TcShape : int {
                  //                             no split-k; clusters of 4 CTAs over 3 Hadamard blocks)
   kN96,          // BN=96,  RG=1, KA=2, XR=128 (n and shard edges multiples of 384)
   kN96R2,        // BN=96,  RG=2, KA=2, XR=128 (n and shard edges multiples of 384)
-  kLast = kN96R2,
+  kN32SmallK8,   // BN=32,  RG=1, KA=8, XR=32  (m <= 32, k a multiple of 512, no split-k)
+  kN64SmallK4,   // BN=64,  RG=1, KA=4, XR=32  (m <= 32, k/128 even, no split-k)
+  kLast = kN64SmallK4,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

@@ -98,6 +98,8 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN96SmallK4: return {96, 4, 32, 1, 1};
     case TcShape::kN96: return {96, 2, 128, 1, 1};
     case TcShape::kN96R2: return {96, 2, 128, 1, 2};
+    case TcShape::kN32SmallK8: return {32, 8, 32, 1, 1};
+    case TcShape::kN64SmallK4: return {64, 4, 32, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -111,6 +113,10 @@ ShapeDims dims_of(TcShape s) {
 // strips spend more of each SM on the cluster, per-stage synchronisation and
 // the tensor core's 128-row operand reads.
 constexpr double kRel64 = 0.48, kRel32 = 0.43, kRel96 = 0.81;
+// More k per stage for the narrow strips (12288 x 4096 and 2048 x 4096, m = 1
+// to 32): 64-column strips on four atoms, 32-column strips on eight once k
+// holds eight or more such stages (fewer leave too short a pipeline).
+constexpr double kRel64K4 = 0.57, kRel32K8 = 0.48;
 // The same for the full-row (128-row) tiles at 32 < m <= 128: 96 columns
 // against 128 (5120 x 12288, m = 48 to 128).
 constexpr double kRel96Full = 0.76;
@@ -237,17 +243,20 @@ TcShape choose_shape(const GemmArgs& a) {
   if (a.m <= 32) {
     // pick the column width whose grid keeps the most decode throughput busy
     const double r128 = small_batch_rate(a.n / 128, 1.0);
-    const double r64 = small_batch_rate(a.n / 64, kRel64);
-    // 32-column strips use 4 k atoms per stage: k must hold an even number of 128-blocks
+    const double r64 = small_batch_rate(a.n / 64, (a.k / 128) % 2 == 0 ? kRel64K4 : kRel64);
+    // 32-column strips take 4 k atoms per stage (k/128 even) or 8 (k a
+    // multiple of 512 and at least 4096); 64-column strips 4 when k/128 is even
     const bool k4 = (a.k / 128) % 2 == 0;
-    const double r32 = k4 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
+    const bool k8 = a.k % 512 == 0 && a.k >= 4096;
+    const double r32 = k8 ? small_batch_rate(a.n / 32, kRel32K8) : k4 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
     // 96-column strips: clusters of four over three Hadamard blocks
     const double r96 = k4 && edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
     // four k atoms per stage halve the per-stage synchronisation (k must hold
     // an even number of 128-blocks)
     if (r128 >= r96 && r128 >= r64 && r128 >= r32) return k4 ? TcShape::kN128SmallK4 : TcShape::kN128Small;
     if (r96 >= r64 && r96 >= r32) return TcShape::kN96SmallK4;
-    return r64 >= r32 ? TcShape::kN64Small : TcShape::kN32Small;
+    if (r64 >= r32) return k4 ? TcShape::kN64SmallK4 : TcShape::kN64Small;
+    return k8 ? TcShape::kN32SmallK8 : TcShape::kN32Small;
   }
   const bool edges384 = edges_multiple_of(a, 384);
   if (a.m <= 128) {
@@ -305,7 +314,8 @@ bool tc_shape_supported(int shape, const GemmArgs& a) {
   const TcShape s = (TcShape)shape;
   const ShapeDims d = dims_of(s);
   if (d.xr < 128 && a.m > d.xr) return false;  // small-batch shapes hold XR rows
-  if (d.ka == 4 && ((a.k / 128) % 2 != 0 || a.parts > 1)) return false;
+  // several atoms per stage: k must hold whole stages, and no split-k
+  if (d.ka > 2 && ((a.k / 128) % (d.ka / 2) != 0 || a.parts > 1)) return false;
   // n and every shard edge fall on whole CTA spans: lcm(BN, 128) columns (a
   // cluster's span when BN is not a multiple of 128)
   return edges_multiple_of(a, lcm_128(d.bn));

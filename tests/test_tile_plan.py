@@ -7,7 +7,7 @@ import pytest
 from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
-N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2 = range(12)
+N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4 = range(14)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -27,7 +27,8 @@ def test_q_proj_plan(m, want):
 
 
 def test_narrow_and_split_layers():
-    assert plan(16, 12288, 4096)[0] == N32S  # 32 column blocks: 32-column strips on 128 SMs
+    assert plan(16, 12288, 4096)[0] == N32SK8  # 32 column blocks: 32-column strips on 128 SMs, 8 atoms a stage
+    assert plan(16, 2048, 4096)[0] == N32S  # k = 2048: four atoms a stage keep the pipeline long enough
     assert plan(16, 5120, 34816, [0, 17408, 34816])[0] == N128SK4  # 272 blocks fill the GPU at 128 columns
     assert plan(16, 384, 4096)[0] != N32S  # odd k/128: no four-atom tiles
     # split-k down projection: 7 parts of 40 blocks; 256-column CTAs need fewer waves
