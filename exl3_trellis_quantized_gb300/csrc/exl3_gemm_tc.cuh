@@ -707,6 +707,9 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN96R2: return launch_tc_variant<BITS, CB, 96, 2, 2, 128>(maps, p, stream);
     case TcShape::kN32SmallK8: return launch_tc_variant<BITS, CB, 32, 1, 8, 32>(maps, p, stream);
     case TcShape::kN64SmallK4: return launch_tc_variant<BITS, CB, 64, 1, 4, 32>(maps, p, stream);
+    case TcShape::kN96M64K4: return launch_tc_variant<BITS, CB, 96, 1, 4, 64>(maps, p, stream);
+    case TcShape::kN64M64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 64>(maps, p, stream);
+    case TcShape::kN64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 128>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

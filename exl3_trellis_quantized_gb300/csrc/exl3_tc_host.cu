@@ -100,6 +100,9 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN96R2: return {96, 2, 128, 1, 2};
     case TcShape::kN32SmallK8: return {32, 8, 32, 1, 1};
     case TcShape::kN64SmallK4: return {64, 4, 32, 1, 1};
+    case TcShape::kN96M64K4: return {96, 4, 64, 1, 1};
+    case TcShape::kN64M64K4: return {64, 4, 64, 1, 1};
+    case TcShape::kN64K4: return {64, 4, 128, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -117,6 +120,12 @@ constexpr double kRel64 = 0.48, kRel32 = 0.43, kRel96 = 0.81;
 // to 32): 64-column strips on four atoms, 32-column strips on eight once k
 // holds eight or more such stages (fewer leave too short a pipeline).
 constexpr double kRel64K4 = 0.57, kRel32K8 = 0.48;
+// 256-column, 256-row tiles at 32 < m <= 128 against 128 columns, per column
+// (5120 x 34816, 4096 x 154880): fewer CTAs in whole waves.
+constexpr double kRel256Mid = 1.07;
+// 64-column strips of 128 rows on four k atoms at 64 < m <= 128 against 128
+// columns (12288 x 4096, 4096 x 8192, 5120 x 6144: 0.68 to 0.78).
+constexpr double kRel64Full = 0.7;
 // The same for the full-row (128-row) tiles at 32 < m <= 128: 96 columns
 // against 128 (5120 x 12288, m = 48 to 128).
 constexpr double kRel96Full = 0.76;
@@ -259,10 +268,26 @@ TcShape choose_shape(const GemmArgs& a) {
     return k8 ? TcShape::kN32SmallK8 : TcShape::kN32Small;
   }
   const bool edges384 = edges_multiple_of(a, 384);
+  if (a.m <= 64 && (a.k / 128) % 2 == 0) {
+    // 33 to 64 rows: the narrow strips hold 64 rows on four k atoms a stage,
+    // measured at the small-batch strips' per-SM rates (5120 x 12288 and
+    // 5120 x 6144, m = 33 to 64); 128 columns keep the 128-row tile
+    const double r128 = small_batch_rate(a.n / 128, 1.0);
+    const double r256 = edges256 ? small_batch_rate(a.n / 256, kRel256Mid) : 0.0;
+    const double r96 = edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
+    const double r64 = small_batch_rate(a.n / 64, kRel64K4);
+    if (r256 > r128 && r256 >= r96 && r256 >= r64) return TcShape::kN256R2;
+    if (r128 >= r96 && r128 >= r64) return TcShape::kN128;
+    return r96 >= r64 ? TcShape::kN96M64K4 : TcShape::kN64M64K4;
+  }
   if (a.m <= 128) {
     // as for small batches: 96-column tiles put a 96-block layer on 128 SMs
     const double r128 = small_batch_rate(a.n / 128, 1.0);
+    const double r256 = edges256 ? small_batch_rate(a.n / 256, kRel256Mid) : 0.0;
     const double r96 = edges384 ? small_batch_rate(a.n / 96, kRel96Full) : 0.0;
+    const double r64 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 64, kRel64Full) : 0.0;
+    if (r256 > r128 && r256 >= r96 && r256 >= r64) return TcShape::kN256R2;
+    if (r64 > r128 && r64 > r96) return TcShape::kN64K4;
     return r96 > r128 ? TcShape::kN96 : TcShape::kN128;
   }
   // Larger batches: least estimated time over whole waves.  Per-CTA costs are

@@ -226,7 +226,7 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     need |= {10, 11} if all(w % 384 == 0 for w in widths) else set()
     if not split and (k // 128) % 2 == 0:
-        need |= {0, 8, 13} | ({9} if all(w % 384 == 0 for w in widths) else set())
+        need |= {0, 8, 13, 15, 16} | ({9, 14} if all(w % 384 == 0 for w in widths) else set())
     if not split and k % 512 == 0:
         need |= {12}
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"

@@ -7,7 +7,8 @@ import pytest
 from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
-N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4 = range(14)
+(N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
+ N64M64K4, N64K4) = range(17)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -17,13 +18,23 @@ def plan(m, k, n, cols=None, split=False):
 
 @pytest.mark.parametrize("m,want", [
     (1, (N96SK4, -1, 0, 0, 0)), (16, (N96SK4, -1, 0, 0, 0)),  # 96 column blocks: 96-column strips, 128 SMs
-    (64, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
+    (48, (N96M64K4, -1, 0, 0, 0)), (64, (N96M64K4, -1, 0, 0, 0)),  # 64-row strips, four atoms a stage
+    (128, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
     (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
     (1024, (N256R2P, N128R2, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 80 256x128 tiles
     (4096, (N256R2P, N128, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 32 128x128 tiles
 ])
 def test_q_proj_plan(m, want):
     assert plan(m, 5120, 12288) == want
+
+
+@pytest.mark.parametrize("m,k,n,cols,want", [
+    (64, 12288, 4096, None, N64M64K4), (100, 12288, 4096, None, N64K4),  # narrow: 64-column strips, four atoms
+    (128, 5120, 6144, None, N64K4), (100, 5120, 12288, None, N96),
+    (48, 5120, 34816, [0, 17408, 34816], N256R2), (128, 4096, 154880, None, N256R2),  # wide: 256-column tiles
+])
+def test_mid_batch_plan(m, k, n, cols, want):
+    assert plan(m, k, n, cols)[0] == want
 
 
 def test_narrow_and_split_layers():
