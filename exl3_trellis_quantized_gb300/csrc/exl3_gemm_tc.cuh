@@ -13,8 +13,8 @@
 // decodes half of the columns and copies its half of the decoded operand into
 // the partner's shared memory, so every decoded weight feeds 2*RG*128 rows.
 // A pair launch may cover only whole waves of pair tiles (numbered row pair
-// major), the rest going to a second launch of smaller tiles (row_base /
-// col_base), see exl3_tc_host.cu.
+// major), the rest going to a second launch of smaller tiles or 128-column
+// pairs (row_base / col_base), see exl3_tc_host.cu.
 //
 // Shared memory holds three rings, each with its own depth: rotated
 // activations (NX slots, RG row groups of KA swizzle atoms of 64 k), decoded

@@ -131,6 +131,11 @@ constexpr double kRel64Full = 0.7;
 constexpr double kRel96Full = 0.76;
 
 constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P = 1.33, kCost96R2 = 0.91;
+// A 128-row, 64-column strip CTA in the split-off last wave of a pair launch,
+// where it runs alone and its decode sets its time: about half of a 128 x 128
+// CTA (GB300, 5120 x 12288 at m = 4096: 64 such CTAs in place of 32 of 128 x
+// 128 took the call from 345.5 to 337.2 us).
+constexpr double kCost64K4 = 0.5;
 
 // Split-k at m <= 128: a 256-column CTA over a k part costs this many 128-column
 // CTAs (decode-bound; its per-stage synchronisation, prologue and epilogue are
@@ -187,7 +192,8 @@ bool edges_multiple_of(const GemmArgs& a, int64_t span) {
 // CTAs fills ceil(C / SMs) waves; when the last is partial its R CTAs (R / 2
 // pair tiles, the last ones in row-pair-major order, so the final columns of
 // the final row pair) can instead run as a second launch of smaller tiles
-// that spread over the whole GPU.  Every shape computes each element with the
+// (or of 128-column pairs, which still share the decode of each weight over
+// 512 rows) that spread over the whole GPU.  Every shape computes each element with the
 // same k16 steps, so the split changes no byte.  The plan is taken when the
 // smaller tiles' waves cost less than the pair wave they replace (costs as in
 // choose_shape).
@@ -215,18 +221,24 @@ TailPlan plan_tail(const GemmArgs& a, TcShape shape) {
   ta.row_base = (nrp - 1) * rows_per_tile;
   ta.col_base = (ncol - tail_tiles) * d.bn;
   const int64_t rows = a.m - ta.row_base, cols = tail_tiles * d.bn;
+  // the tail's tiles: 128 x 128, 256 x 128, 256 x 256, pairs of 256 x 128
+  // (each CTA of a pair decodes half of the 128 columns for 512 rows), or
+  // 128-row strips of 64 columns (four k atoms a stage; k/128 even)
   struct Option {
     TcShape shape;
-    int64_t rows_per_cta, bn;
+    int64_t rows_per_cta, bn, pair;
     double cost;
   };
-  const Option opts[3] = {{TcShape::kN128, 128, 128, kCost128},
-                          {TcShape::kN128R2, 256, 128, 1.0},
-                          {TcShape::kN256R2, 256, 256, kCost256}};
+  const Option opts[5] = {{TcShape::kN128, 128, 128, 1, kCost128},
+                          {TcShape::kN128R2, 256, 128, 1, 1.0},
+                          {TcShape::kN256R2, 256, 256, 1, kCost256},
+                          {TcShape::kN128R2P, 256, 128, 2, kCost128P},
+                          {TcShape::kN64K4, 128, 64, 1, kCost64K4}};
   double best = 1e300;
   for (const Option& o : opts) {
     if (cols % o.bn != 0 || ta.col_base % o.bn != 0 || !tc_shape_supported((int)o.shape, ta)) continue;
-    const double tt = large_batch_time((rows + o.rows_per_cta - 1) / o.rows_per_cta * (cols / o.bn), o.cost);
+    const int64_t span = o.rows_per_cta * o.pair;
+    const double tt = large_batch_time((rows + span - 1) / span * o.pair * (cols / o.bn), o.cost);
     if (tt < best) {
       best = tt;
       t.tail = o.shape;

@@ -282,7 +282,8 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
  * or exl3_gemm_splitk call (split = 1) of the given sizes, computed on the host
  * with no launch (the SM count of the current device, 152 when there is none).
  * out[0] = tile shape (numbered as in exl3_test_gemm_shape); for a pair shape
- * whose partial last wave runs as a second launch of smaller tiles, out[1] =
+ * whose partial last wave runs as a second launch of smaller tiles (or of
+ * 128-column pairs), out[1] =
  * that launch's shape, out[2] = pair tiles of the first launch, out[3] and
  * out[4] = first row and first column of the second launch; otherwise
  * out[1] = -1 and out[2..4] = 0.  EXL3_EINVAL for invalid sizes or shard map.

@@ -319,10 +319,11 @@ def test_full_size_sampled(name, k, widths, bits, cb, m, split):
 SPLIT_CASES = [
     # k, shard widths, bits, codebook, m: pair launches whose partial last wave
     # is split off into a second launch of smaller tiles on 152 SMs
-    (256, [12288], 4, 1, 1024),  # 192 pair CTAs: 40 of them become 256-row x 128-column tiles
+    (256, [12288], 4, 1, 1024),  # 192 pair CTAs: 40 of them become 40 pairs of 256-row x 128-column tiles
     (256, [10240, 2048], 3, 0, 1024),  # the split-off columns span both shards
-    (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 128 x 128 tiles
-    (256, [7680], 4, 1, 3000),  # a ragged last row pair (440 rows) in the split-off tiles
+    (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 64 strips of 128 rows x 64 columns
+    (256, [7680], 4, 1, 3000),  # a ragged last row pair (440 rows) in the split-off pairs
+    (256, [27648], 4, 1, 768),  # 432 pair CTAs: 128 become 256 x 128 tiles (128 x 128 ones for 128-column pairs)
 ]
 
 

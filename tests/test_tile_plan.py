@@ -21,8 +21,8 @@ def plan(m, k, n, cols=None, split=False):
     (48, (N96M64K4, -1, 0, 0, 0)), (64, (N96M64K4, -1, 0, 0, 0)),  # 64-row strips, four atoms a stage
     (128, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
     (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
-    (1024, (N256R2P, N128R2, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 80 256x128 tiles
-    (4096, (N256R2P, N128, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 32 128x128 tiles
+    (1024, (N256R2P, N128R2P, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 40 pairs of 256x128 tiles
+    (4096, (N256R2P, N64K4, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 64 strips of 128 x 64
 ])
 def test_q_proj_plan(m, want):
     assert plan(m, 5120, 12288) == want
@@ -60,7 +60,7 @@ def test_split_last_wave_invariants(m, k, n):
     assert (2 * primary) % SMS == 0, "the first launch is whole waves"
     assert row_base == (nrp - 1) * rows_per_pair_tile, "the split-off tiles are in the last row pair"
     assert (n - col_base) // bn == total_tiles - primary, "the second launch covers exactly the tiles left"
-    assert col_base % bn == 0 and tail in (N128, N128R2, N256R2)
+    assert col_base % bn == 0 and tail in (N128, N128R2, N256R2, N128R2P, N64K4)
 
 
 def test_plan_rejects_invalid():
