@@ -247,7 +247,6 @@ def run_gpu(args, wl_name):
     torch.cuda.synchronize()
 
     # --- device-resident timed region -------------------------------------
-    per_m = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in ms]
     per_m_ms = [0.0] * len(ms)
     clocks = ClockSampler(local)
     if world > 1:
@@ -269,14 +268,19 @@ def run_gpu(args, wl_name):
     clk = clocks.stop()
     elapsed = max_over_ranks(t0.elapsed_time(t1) / 1e3, dev)
 
-    # per-batch-size breakdown, measured separately (same launches, events around each)
+    # per-batch-size breakdown, measured separately (same launches, events
+    # around each; no host synchronisation between steps, so the host stays
+    # ahead of the device as in the timed region)
     reps = max(3, min(args.steps, 50))
     per_m_samples = [[] for _ in ms]
-    for _ in range(reps):
-        step(per_m)
-        torch.cuda.synchronize()
+    bd_ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in ms]
+             for _ in range(reps)]
+    for j in range(reps):
+        step(bd_ev[j])
+    torch.cuda.synchronize()
+    for j in range(reps):
         for i in range(len(ms)):
-            t_ms = per_m[i][0].elapsed_time(per_m[i][1])
+            t_ms = bd_ev[j][i][0].elapsed_time(bd_ev[j][i][1])
             per_m_ms[i] += t_ms
             per_m_samples[i].append(t_ms)
     per_m_s = [v / reps / 1e3 for v in per_m_ms]

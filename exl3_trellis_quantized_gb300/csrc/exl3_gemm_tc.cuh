@@ -710,6 +710,7 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN96M64K4: return launch_tc_variant<BITS, CB, 96, 1, 4, 64>(maps, p, stream);
     case TcShape::kN64M64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 64>(maps, p, stream);
     case TcShape::kN64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 128>(maps, p, stream);
+    case TcShape::kN32K4: return launch_tc_variant<BITS, CB, 32, 1, 4, 128>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

@@ -106,8 +106,10 @@ enum class TcShape : int {
   kN64SmallK4,   // BN=64,  RG=1, KA=4, XR=32  (m <= 32, k/128 even, no split-k)
   kN96M64K4,     // BN=96,  RG=1, KA=4, XR=64  (m <= 64, k/128 even, no split-k, 384-aligned edges)
   kN64M64K4,     // BN=64,  RG=1, KA=4, XR=64  (m <= 64, k/128 even, no split-k)
-  kN64K4,        // BN=64,  RG=1, KA=4, XR=128 (m <= 128, k/128 even, no split-k)
-  kLast = kN64K4,
+  kN64K4,        // BN=64,  RG=1, KA=4, XR=128 (m <= 128, split-off tails; k/128 even, no split-k)
+  kN32K4,        // BN=32,  RG=1, KA=4, XR=128 (m <= 128 on narrow layers, split-off tails; k/128 even,
+                 //                             no split-k)
+  kLast = kN32K4,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

@@ -103,6 +103,7 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN96M64K4: return {96, 4, 64, 1, 1};
     case TcShape::kN64M64K4: return {64, 4, 64, 1, 1};
     case TcShape::kN64K4: return {64, 4, 128, 1, 1};
+    case TcShape::kN32K4: return {32, 4, 128, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -126,6 +127,12 @@ constexpr double kRel256Mid = 1.07;
 // 64-column strips of 128 rows on four k atoms at 64 < m <= 128 against 128
 // columns (12288 x 4096, 4096 x 8192, 5120 x 6144: 0.68 to 0.78).
 constexpr double kRel64Full = 0.7;
+// 32-column strips of 128 rows on four k atoms at 32 < m <= 128, per SM
+// against a 128-column CTA: layers with few 128-column blocks get twice the
+// CTAs of the 64-column strips (12288 x 4096: 43.6 to 43.9 us against 49.7 to
+// 53.1 at m = 48 to 128; where 64-column strips already fill the GPU, as on
+// 4096 x 8192 and 5120 x 6144, they stay faster).
+constexpr double kRel32Full = 0.4;
 // The same for the full-row (128-row) tiles at 32 < m <= 128: 96 columns
 // against 128 (5120 x 12288, m = 48 to 128).
 constexpr double kRel96Full = 0.76;
@@ -136,6 +143,10 @@ constexpr double kCost128 = 0.87, kCost128P = 0.93, kCost256 = 1.49, kCost256P =
 // CTA (GB300, 5120 x 12288 at m = 4096: 64 such CTAs in place of 32 of 128 x
 // 128 took the call from 345.5 to 337.2 us).
 constexpr double kCost64K4 = 0.5;
+// The same for 32-column strips (5120 x 12288 at m = 4096: 128 of them in place
+// of 64 of 64 columns, 339.0 to 334.5 us; wider tails lose, as their grids
+// need several waves).
+constexpr double kCost32K4 = 0.3;
 
 // Split-k at m <= 128: a 256-column CTA over a k part costs this many 128-column
 // CTAs (decode-bound; its per-stage synchronisation, prologue and epilogue are
@@ -223,17 +234,18 @@ TailPlan plan_tail(const GemmArgs& a, TcShape shape) {
   const int64_t rows = a.m - ta.row_base, cols = tail_tiles * d.bn;
   // the tail's tiles: 128 x 128, 256 x 128, 256 x 256, pairs of 256 x 128
   // (each CTA of a pair decodes half of the 128 columns for 512 rows), or
-  // 128-row strips of 64 columns (four k atoms a stage; k/128 even)
+  // 128-row strips of 64 or 32 columns (four k atoms a stage; k/128 even)
   struct Option {
     TcShape shape;
     int64_t rows_per_cta, bn, pair;
     double cost;
   };
-  const Option opts[5] = {{TcShape::kN128, 128, 128, 1, kCost128},
+  const Option opts[6] = {{TcShape::kN128, 128, 128, 1, kCost128},
                           {TcShape::kN128R2, 256, 128, 1, 1.0},
                           {TcShape::kN256R2, 256, 256, 1, kCost256},
                           {TcShape::kN128R2P, 256, 128, 2, kCost128P},
-                          {TcShape::kN64K4, 128, 64, 1, kCost64K4}};
+                          {TcShape::kN64K4, 128, 64, 1, kCost64K4},
+                          {TcShape::kN32K4, 128, 32, 1, kCost32K4}};
   double best = 1e300;
   for (const Option& o : opts) {
     if (cols % o.bn != 0 || ta.col_base % o.bn != 0 || !tc_shape_supported((int)o.shape, ta)) continue;
@@ -288,8 +300,10 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r256 = edges256 ? small_batch_rate(a.n / 256, kRel256Mid) : 0.0;
     const double r96 = edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
     const double r64 = small_batch_rate(a.n / 64, kRel64K4);
-    if (r256 > r128 && r256 >= r96 && r256 >= r64) return TcShape::kN256R2;
-    if (r128 >= r96 && r128 >= r64) return TcShape::kN128;
+    const double r32 = small_batch_rate(a.n / 32, kRel32Full);  // 128-row strips
+    if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
+    if (r128 >= r96 && r128 >= r64 && r128 >= r32) return TcShape::kN128;
+    if (r32 > r96 && r32 > r64) return TcShape::kN32K4;
     return r96 >= r64 ? TcShape::kN96M64K4 : TcShape::kN64M64K4;
   }
   if (a.m <= 128) {
@@ -298,7 +312,9 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r256 = edges256 ? small_batch_rate(a.n / 256, kRel256Mid) : 0.0;
     const double r96 = edges384 ? small_batch_rate(a.n / 96, kRel96Full) : 0.0;
     const double r64 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 64, kRel64Full) : 0.0;
-    if (r256 > r128 && r256 >= r96 && r256 >= r64) return TcShape::kN256R2;
+    const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32Full) : 0.0;
+    if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
+    if (r32 > r128 && r32 > r96 && r32 > r64) return TcShape::kN32K4;
     if (r64 > r128 && r64 > r96) return TcShape::kN64K4;
     return r96 > r128 ? TcShape::kN96 : TcShape::kN128;
   }

@@ -266,11 +266,12 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
  *         64 rows with four (m <= 64, k/128 even, no split-k, n and shard
  *         edges multiples of 384), 15 = 64-column strips holding 64 rows with
  *         four (m <= 64, k/128 even, no split-k), 16 = 64-column strips of
- *         128 rows with four (m <= 128, k/128 even, no split-k).
+ *         128 rows with four (k/128 even, no split-k), 17 = 32-column strips
+ *         of 128 rows with four (k/128 even, no split-k).
  * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
  * call (the conditions in parentheses).
  */
-#define EXL3_TEST_TILE_SHAPES 17
+#define EXL3_TEST_TILE_SHAPES 18
 exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
                                    const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                    const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,

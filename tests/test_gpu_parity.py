@@ -226,7 +226,7 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     need = {1, 2, 3, 4, 6} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     need |= {10, 11} if all(w % 384 == 0 for w in widths) else set()
     if not split and (k // 128) % 2 == 0:
-        need |= {0, 8, 13, 15, 16} | ({9, 14} if all(w % 384 == 0 for w in widths) else set())
+        need |= {0, 8, 13, 15, 16, 17} | ({9, 14} if all(w % 384 == 0 for w in widths) else set())
     if not split and k % 512 == 0:
         need |= {12}
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
@@ -321,7 +321,8 @@ SPLIT_CASES = [
     # is split off into a second launch of smaller tiles on 152 SMs
     (256, [12288], 4, 1, 1024),  # 192 pair CTAs: 40 of them become 40 pairs of 256-row x 128-column tiles
     (256, [10240, 2048], 3, 0, 1024),  # the split-off columns span both shards
-    (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 64 strips of 128 rows x 64 columns
+    (256, [6144, 6144], 5, 2, 4096),  # 768 pair CTAs: 8 become 128 strips of 128 rows x 32 columns
+    (256, [4608], 3, 2, 2184),  # 180 pair CTAs = 152 + 28: 64-column strips over a ragged 136 rows
     (256, [7680], 4, 1, 3000),  # a ragged last row pair (440 rows) in the split-off pairs
     (256, [27648], 4, 1, 768),  # 432 pair CTAs: 128 become 256 x 128 tiles (128 x 128 ones for 128-column pairs)
 ]

@@ -8,7 +8,7 @@ from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
 (N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
- N64M64K4, N64K4) = range(17)
+ N64M64K4, N64K4, N32K4) = range(18)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -22,14 +22,15 @@ def plan(m, k, n, cols=None, split=False):
     (128, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
     (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
     (1024, (N256R2P, N128R2P, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 40 pairs of 256x128 tiles
-    (4096, (N256R2P, N64K4, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 64 strips of 128 x 64
+    (4096, (N256R2P, N32K4, 380, 3584, 11264)),  # 768 = 5 x 152 + 8: the 8 become 128 strips of 128 x 32
 ])
 def test_q_proj_plan(m, want):
     assert plan(m, 5120, 12288) == want
 
 
 @pytest.mark.parametrize("m,k,n,cols,want", [
-    (64, 12288, 4096, None, N64M64K4), (100, 12288, 4096, None, N64K4),  # narrow: 64-column strips, four atoms
+    (64, 12288, 4096, None, N32K4), (100, 12288, 4096, None, N32K4),  # 32 blocks: 128 strips of 32 columns
+    (64, 4096, 8192, None, N64M64K4), (100, 4096, 8192, None, N64K4),  # 64 blocks: 64-column strips, four atoms
     (128, 5120, 6144, None, N64K4), (100, 5120, 12288, None, N96),
     (48, 5120, 34816, [0, 17408, 34816], N256R2), (128, 4096, 154880, None, N256R2),  # wide: 256-column tiles
 ])
@@ -60,7 +61,7 @@ def test_split_last_wave_invariants(m, k, n):
     assert (2 * primary) % SMS == 0, "the first launch is whole waves"
     assert row_base == (nrp - 1) * rows_per_pair_tile, "the split-off tiles are in the last row pair"
     assert (n - col_base) // bn == total_tiles - primary, "the second launch covers exactly the tiles left"
-    assert col_base % bn == 0 and tail in (N128, N128R2, N256R2, N128R2P, N64K4)
+    assert col_base % bn == 0 and tail in (N128, N128R2, N256R2, N128R2P, N64K4, N32K4)
 
 
 def test_plan_rejects_invalid():
