@@ -166,3 +166,11 @@ def make_routing(num_tokens: int, num_experts: int, topk: int, block: int, seed:
         ids[at * block:at * block] = [pad] * block
     return Routing(num_tokens=num_tokens, topk=topk, block=block, topk_ids=topk_ids,
                    sorted_ids=torch.tensor(ids, dtype=torch.int32), block_expert=torch.tensor(blocks, dtype=torch.int32))
+
+
+def make_topk_weights(num_tokens: int, topk: int, seed: int) -> torch.Tensor:
+    """Router weights of each token's top-k slots: float32 [num_tokens, topk],
+    positive and normalised to sum to 1 per token."""
+    g = torch.Generator().manual_seed(seed)
+    w = torch.rand((num_tokens, topk), generator=g, dtype=torch.float32) + 0.05
+    return w / w.sum(dim=1, keepdim=True)

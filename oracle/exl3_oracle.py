@@ -449,3 +449,34 @@ def moe_linear(x, sorted_ids, block_expert, block: int, topk: int, trellis, bits
         y[b * block:(b + 1) * block] = linear(xb, np.asarray(trellis[e]), bits, cb, np.asarray(suh[e]),
                                               np.asarray(svh[e]), shard_cols)
     return y
+
+
+def moe_combine(y_rows, sorted_ids, block_expert, block: int, topk: int, weights, num_tokens: int,
+                num_experts: int) -> np.ndarray:
+    """The weighted combine of each token's top-k expert outputs, float64
+    [num_tokens, N].
+
+    Reading (the pages run the routed experts as a grouped GEMM over
+    block-aligned rows and leave the combine to the caller: cuda-exl3 README,
+    "What is supported", "MoE notes"): out[t] = sum over the slots s of token
+    t, in ascending s, of weights[t, s] * y_rows[r], where r is the padded row
+    of a live block (expert id in [0, num_experts)) whose sorted_ids entry is
+    the pair t * topk + s.  A pair with no such row adds nothing; padding rows
+    and rows of blocks of no expert are never read."""
+    y = np.asarray(y_rows, dtype=np.float64)
+    w = np.asarray(weights, dtype=np.float64).reshape(num_tokens, topk)
+    ids = np.asarray(sorted_ids)
+    experts = np.asarray(block_expert)
+    row_of = {}
+    for r in range(len(ids)):
+        e = int(experts[r // block])
+        p = int(ids[r])
+        if 0 <= e < num_experts and 0 <= p < num_tokens * topk:
+            row_of[p] = r
+    out = np.zeros((num_tokens, y.shape[1]))
+    for t in range(num_tokens):
+        for s in range(topk):
+            r = row_of.get(t * topk + s)
+            if r is not None:
+                out[t] += w[t, s] * y[r]
+    return out

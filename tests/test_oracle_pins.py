@@ -402,3 +402,84 @@ def test_moe_input_transform_follows_topk_choices():
         t, j = divmod(int(pair), r.topk)
         e = int(r.topk_ids[t, j])
         assert np.array_equal(xh[:, row], o.input_transform(x[t][None], layer.suh[e].double().numpy())[:, 0])
+
+
+# ---------------------------------------------------------------------------
+# Mixture of experts: the weighted combine of a token's top-k rows
+# ---------------------------------------------------------------------------
+
+
+def _moe_rows(layer, r, x):
+    return o.moe_linear(x, r.sorted_ids.numpy(), r.block_expert.numpy(), r.block, r.topk, layer.trellis.numpy(),
+                        layer.bits, layer.codebook, layer.suh.double().numpy(), layer.svh.double().numpy(),
+                        layer.shard_cols)
+
+
+def _combine(y, r, w, experts, block_expert=None):
+    be = r.block_expert.numpy() if block_expert is None else block_expert
+    return o.moe_combine(y, r.sorted_ids.numpy(), be, r.block, r.topk, w, r.num_tokens, experts)
+
+
+def test_moe_combine_is_the_weighted_sum_of_dense_experts():
+    """out[t] = sum_j w[t, j] * layer_{topk_ids[t, j]}(x[t]), with the experts taken
+    from the routing's own top-k table, not from the block layout (the rows of
+    blocks of no expert are NaN in the grouped output: reading one would show)."""
+    layer, r, x = _moe_case()
+    w = synthetic.make_topk_weights(r.num_tokens, r.topk, seed=81).double().numpy()
+    out = _combine(_moe_rows(layer, r, x), r, w, 5)
+    for t in range(r.num_tokens):
+        want = np.zeros(out.shape[1])
+        for j in range(r.topk):
+            e = int(r.topk_ids[t, j])
+            want += w[t, j] * o.linear(x[t][None], layer.trellis[e].numpy(), layer.bits, layer.codebook,
+                                       layer.suh[e].double().numpy(), layer.svh[e].double().numpy(),
+                                       layer.shard_cols)[0]
+        assert np.allclose(out[t], want, rtol=0, atol=1e-12)
+
+
+def test_moe_combine_one_hot_weights_gather_the_slot_row():
+    layer, r, x = _moe_case(seed=91, tokens=6, experts=4, topk=3, block=4)
+    y = _moe_rows(layer, r, x)
+    ids = r.sorted_ids.numpy()
+    for j in range(r.topk):
+        w = np.zeros((r.num_tokens, r.topk))
+        w[:, j] = 1.0
+        out = _combine(y, r, w, 4)
+        for t in range(r.num_tokens):
+            (row,) = np.nonzero(ids == t * r.topk + j)[0]
+            assert np.array_equal(out[t], y[row])
+
+
+def test_moe_combine_ignores_the_block_layout():
+    """The same choices with or without blocks of no expert between the live
+    ones give the same combine."""
+    layer = synthetic.make_moe_layer(256, [128, 128], 3, 1, 5, seed=101)
+    x = synthetic.make_x(7, 256, seed=102).double().numpy()
+    w = synthetic.make_topk_weights(7, 2, seed=103).double().numpy()
+    outs = []
+    for empty in (0, 3):
+        r = synthetic.make_routing(7, 5, 2, 4, seed=104, empty_blocks=empty)
+        outs.append(_combine(_moe_rows(layer, r, x), r, w, 5))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_moe_combine_drops_pairs_without_a_live_row():
+    """Marking a live block as no expert (-1, or an id past the last expert)
+    removes exactly its pairs' terms."""
+    layer, r, x = _moe_case(seed=111)
+    w = synthetic.make_topk_weights(r.num_tokens, r.topk, seed=112).double().numpy()
+    y = _moe_rows(layer, r, x)
+    full = _combine(y, r, w, 5)
+    be = r.block_expert.numpy().copy()
+    b = int(np.nonzero(be >= 0)[0][0])
+    for mark in (-1, 5):
+        dropped = be.copy()
+        dropped[b] = mark
+        got = _combine(y, r, w, 5, dropped)
+        want = full.copy()
+        for row in range(b * r.block, (b + 1) * r.block):
+            pair = int(r.sorted_ids[row])
+            if pair < r.num_tokens * r.topk:
+                t, j = divmod(pair, r.topk)
+                want[t] -= w[t, j] * y[row]
+        assert np.allclose(got, want, rtol=0, atol=1e-12)
