@@ -781,11 +781,34 @@ def run_moe(args):
         torch.cuda.synchronize()
         tg = ev[0].elapsed_time(ev[1]) / 1e3 / (3 * reps)
         del g
+        # the weighted combine of each token's top-k rows, on rows of the
+        # hidden width (the down projection's output), replayed from a graph
+        yd = synthetic.make_x(run["rows"], hid, seed=1204).to(dev)
+        wt = synthetic.make_topk_weights(run["t"], topk, seed=1205).to(dev)
+        table = torch.empty(run["t"] * topk, dtype=torch.int32, device=dev)
+        comb = torch.empty((run["t"], hid), dtype=torch.bfloat16, device=dev)
+        E.moe_combine(yd, run["ids"], run["be"], run["block"], ne, wt, topk, out=comb, pair_rows=table)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g, stream=cap):
+                for i in range(reps):
+                    E.moe_combine(yd, run["ids"], run["be"], run["block"], ne, wt, topk, out=comb, pair_rows=table)
+        g.replay()
+        torch.cuda.synchronize()
+        ev[0].record()
+        for _ in range(3):
+            g.replay()
+        ev[1].record()
+        torch.cuda.synchronize()
+        tc = ev[0].elapsed_time(ev[1]) / 1e3 / (3 * reps)
+        del g
+        comb_bytes = (run["t"] * topk + run["t"]) * hid * 2  # the routed rows read, the combined rows written
         sol = max(run["bytes"] / (peaks["hbm_gbs"] * 1e9), run["flops"] / (peaks["bf16_tflops"] * 1e12))
         per.append({"tokens": run["t"], "block": run["block"], "rows": run["rows"], "live_blocks": run["blocks"],
                     "us": round(t * 1e6, 2), "graph_us": round(tg * 1e6, 2),
                     "GBps_touched_experts": round(run["bytes"] / tg / 1e9, 1),
-                    "pct_roofline": round(100.0 * sol / tg, 2)})
+                    "pct_roofline": round(100.0 * sol / tg, 2),
+                    "combine_us": round(tc * 1e6, 2), "combine_GBps": round(comb_bytes / tc / 1e9, 1)})
     sol_step = sum(max(r_["bytes"] / (peaks["hbm_gbs"] * 1e9), r_["flops"] / (peaks["bf16_tflops"] * 1e12))
                    for r_ in runs)
     return {

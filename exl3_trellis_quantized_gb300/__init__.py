@@ -18,6 +18,7 @@ from .binding import (  # noqa: F401
     lib,
     linear,
     set_autotune,
+    moe_combine,
     moe_gemm,
     moe_input_transform,
     splitk_parts,

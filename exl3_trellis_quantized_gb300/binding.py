@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
     L.exl3_moe_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, i32, i32, vp, ctypes.c_int,
                                 i64, vp]
     L.exl3_moe_gemm.restype = ctypes.c_int
+    L.exl3_moe_combine.argtypes = [vp, ctypes.c_int, i64, i64, vp, vp, i32, i32, vp, i64, i32, vp, vp, ctypes.c_int, vp]
+    L.exl3_moe_combine.restype = ctypes.c_int
     L.exl3_input_transform_swiglu.argtypes = [vp, ctypes.c_int, i64, i64, vp, i32, vp, vp]
     L.exl3_input_transform_swiglu.restype = ctypes.c_int
     L.exl3_gemm.argtypes = [vp, i64, i64, vp, i32, ctypes.c_int, vp, vp, i32, vp, ctypes.c_int, i64, vp]
@@ -230,6 +232,38 @@ def moe_gemm(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.
     st = lib().exl3_moe_gemm(_ptr(xh), rows, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(block_expert),
                              int(block), e, _ptr(out), _BF16 if out.dtype == torch.bfloat16 else _F16, n, _stream(xh))
     _check(st, "exl3_moe_gemm")
+    return out
+
+
+def moe_combine(y: torch.Tensor, sorted_ids: torch.Tensor, block_expert: torch.Tensor, block: int,
+                num_experts: int, weights: torch.Tensor, topk: int, out_dtype=torch.bfloat16,
+                out: Optional[torch.Tensor] = None, pair_rows: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Weighted sum of each token's top-k rows of a grouped GEMM's output:
+    y [rows, n] (bf16/fp16), weights fp32 [tokens, topk] -> out [tokens, n].
+    pair_rows is int32 [tokens * topk] scratch (allocated when not given)."""
+    if y.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("y must be bf16 or fp16")
+    _need(y, y.dtype, "y")
+    _need(sorted_ids, torch.int32, "sorted_ids")
+    _need(block_expert, torch.int32, "block_expert")
+    _need(weights, torch.float32, "weights")
+    rows, n = y.shape
+    num_tokens = weights.shape[0]
+    if weights.shape != (num_tokens, topk):
+        raise ValueError("weights must be [tokens, topk]")
+    if out is None:
+        out = torch.empty((num_tokens, n), dtype=out_dtype, device=y.device)
+    if out.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("output must be bf16 or fp16")
+    _need(out, out.dtype, "out")
+    if pair_rows is None:
+        pair_rows = torch.empty(max(1, num_tokens * topk), dtype=torch.int32, device=y.device)
+    _need(pair_rows, torch.int32, "pair_rows")
+    st = lib().exl3_moe_combine(_ptr(y), _BF16 if y.dtype == torch.bfloat16 else _F16, rows, n, _ptr(sorted_ids),
+                                _ptr(block_expert), int(block), int(num_experts), _ptr(weights), num_tokens,
+                                int(topk), _ptr(pair_rows), _ptr(out), _BF16 if out.dtype == torch.bfloat16 else _F16,
+                                _stream(y))
+    _check(st, "exl3_moe_combine")
     return out
 
 

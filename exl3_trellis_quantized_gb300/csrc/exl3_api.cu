@@ -135,6 +135,22 @@ exl3_status_t exl3_moe_gemm(const uint16_t* xh, int64_t rows, int64_t k, const i
   return cuda_status(exl3::launch_moe_gemm_tc(a, bits, cb, block, static_cast<cudaStream_t>(stream)), "exl3_moe_gemm");
 }
 
+exl3_status_t exl3_moe_combine(const void* y, exl3_dtype_t y_dtype, int64_t rows, int64_t n,
+                               const int32_t* sorted_ids, const int32_t* block_expert, int32_t block,
+                               int32_t num_experts, const float* weights, int64_t num_tokens, int32_t topk,
+                               int32_t* pair_rows, void* out, exl3_dtype_t out_dtype, void* stream) {
+  if (rows < 0 || rows > kMaxRows || num_tokens < 0 || num_tokens > kMaxRows || !valid_kn(n)) return EXL3_EINVAL;
+  if (!valid_dtype(y_dtype) || !valid_dtype(out_dtype) || topk < 1 || topk > 64) return EXL3_EINVAL;
+  if (!valid_moe_block(block) || rows % block || num_experts < 1) return EXL3_EINVAL;
+  if (num_tokens == 0) return EXL3_OK;
+  if (!aligned16(out) || weights == nullptr || pair_rows == nullptr) return EXL3_EINVAL;
+  if (rows > 0 && (!aligned16(y) || sorted_ids == nullptr || block_expert == nullptr)) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_moe_combine(y, y_dtype == EXL3_BF16, rows, n, sorted_ids, block_expert, block,
+                                              num_experts, weights, num_tokens, topk, pair_rows, out,
+                                              out_dtype == EXL3_BF16, static_cast<cudaStream_t>(stream)),
+                     "exl3_moe_combine");
+}
+
 exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis, int32_t bits,
                         exl3_codebook_t cb, const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,
                         void* y, exl3_dtype_t y_dtype, int64_t n, void* stream) {

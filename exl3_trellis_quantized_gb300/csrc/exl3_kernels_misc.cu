@@ -1,4 +1,4 @@
-// exl3_kernels_misc.cu -- the split-k epilogue and the test-only decode kernels.
+// exl3_kernels_misc.cu -- the split-k epilogue, the MoE combine and the test-only decode kernels.
 #include "exl3_device.cuh"
 #include "exl3_launch.h"
 
@@ -68,6 +68,123 @@ cudaError_t launch_splitk_epilogue(const GemmArgs& a, cudaStream_t stream) {
     EXL3_SPLITK_CASE(12) EXL3_SPLITK_CASE(13) EXL3_SPLITK_CASE(14) EXL3_SPLITK_CASE(15) EXL3_SPLITK_CASE(16)
 #undef EXL3_SPLITK_CASE
     default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// MoE combine: the weighted sum of each token's top-k expert rows (the pages
+// run the routed experts as a grouped GEMM and leave this sum to the caller:
+// cuda-exl3 README, "MoE notes").  Two launches, no atomics:
+//   1. every row of a live block whose pair id p lies in [0, tokens * topk)
+//      records pair_rows[p] = row;
+//   2. per token and 8-column chunk, the slots in ascending order: a slot's
+//      entry counts only when it names a row of a live block that holds this
+//      very pair, so entries never written in this call (left from an earlier
+//      call, or garbage) are ignored and the table needs no clearing; the sum
+//      is fp32, w * y added with one fma per slot in slot order, then one
+//      rounding to the output type.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) moe_pair_rows_kernel(const int32_t* __restrict__ sorted_ids, int64_t rows,
+                                                            const int32_t* __restrict__ block_expert,
+                                                            int block_shift, int num_experts, int64_t pairs,
+                                                            int32_t* __restrict__ pair_rows) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += stride) {
+    const int e = block_expert[r >> block_shift];
+    const int64_t p = sorted_ids[r];
+    if (e >= 0 && e < num_experts && p >= 0 && p < pairs) pair_rows[p] = (int32_t)r;
+  }
+}
+
+template <bool Y_BF16>
+__device__ __forceinline__ float row_elem_to_f32(uint32_t e) {
+  return Y_BF16 ? __bfloat162float(__ushort_as_bfloat16((uint16_t)e)) : __half2float(__ushort_as_half((uint16_t)e));
+}
+
+template <bool Y_BF16>
+__global__ void __launch_bounds__(256) moe_combine_kernel(const uint16_t* __restrict__ y, int64_t rows, int64_t n,
+                                                          const int32_t* __restrict__ sorted_ids,
+                                                          const int32_t* __restrict__ block_expert, int block_shift,
+                                                          int num_experts, const float* __restrict__ weights,
+                                                          int64_t num_tokens, int topk,
+                                                          const int32_t* __restrict__ pair_rows,
+                                                          uint16_t* __restrict__ out, bool out_bf16) {
+  const int64_t chunks = n >> 3;
+  const int64_t units = num_tokens * chunks;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < units; u += stride) {
+    const int64_t t = u / chunks;
+    const int64_t c = (u - t * chunks) << 3;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    // eight slots at a time: their table entries, then their checks, then
+    // their rows are each loaded together (three rounds of independent loads
+    // instead of three dependent loads per slot); the sum stays in slot order
+    for (int s0 = 0; s0 < topk; s0 += 8) {
+      int32_t r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) r[j] = s0 + j < topk ? pair_rows[t * topk + s0 + j] : -1;
+      bool live[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        live[j] = r[j] >= 0 && r[j] < rows;
+        if (live[j]) {
+          const int e = block_expert[r[j] >> block_shift];
+          live[j] = (int64_t)sorted_ids[r[j]] == t * topk + s0 + j && e >= 0 && e < num_experts;
+        }
+      }
+      uint4 v[8];
+      float w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (live[j]) {
+          v[j] = *reinterpret_cast<const uint4*>(y + (int64_t)r[j] * n + c);
+          w[j] = weights[t * topk + s0 + j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (!live[j]) continue;
+        const uint32_t vw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(w[j], row_elem_to_f32<Y_BF16>(vw[i] & 0xFFFFu), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(w[j], row_elem_to_f32<Y_BF16>(vw[i] >> 16), acc[2 * i + 1]);
+        }
+      }
+    }
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      o[i] = (uint32_t)f32_to_out(acc[2 * i], out_bf16) | ((uint32_t)f32_to_out(acc[2 * i + 1], out_bf16) << 16);
+    *reinterpret_cast<uint4*>(out + t * n + c) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_moe_combine(const void* y, bool y_bf16, int64_t rows, int64_t n, const int32_t* sorted_ids,
+                               const int32_t* block_expert, int32_t block, int num_experts, const float* weights,
+                               int64_t num_tokens, int32_t topk, int32_t* pair_rows, void* out, bool out_bf16,
+                               cudaStream_t stream) {
+  const int shift = block == 16 ? 4 : block == 32 ? 5 : 7;
+  if (rows > 0) {
+    const int64_t want = (rows + 255) / 256;
+    const int blocks = (int)(want < 152 * 8 ? want : 152 * 8);
+    moe_pair_rows_kernel<<<blocks, 256, 0, stream>>>(sorted_ids, rows, block_expert, shift, num_experts,
+                                                     num_tokens * topk, pair_rows);
+  }
+  if (num_tokens > 0) {
+    const int64_t want = (num_tokens * (n >> 3) + 255) / 256;
+    const int blocks = (int)(want < 152 * 8 ? want : 152 * 8);
+    const uint16_t* yy = static_cast<const uint16_t*>(y);
+    uint16_t* oo = static_cast<uint16_t*>(out);
+    if (y_bf16) {
+      moe_combine_kernel<true><<<blocks, 256, 0, stream>>>(yy, rows, n, sorted_ids, block_expert, shift, num_experts,
+                                                           weights, num_tokens, topk, pair_rows, oo, out_bf16);
+    } else {
+      moe_combine_kernel<false><<<blocks, 256, 0, stream>>>(yy, rows, n, sorted_ids, block_expert, shift,
+                                                            num_experts, weights, num_tokens, topk, pair_rows, oo,
+                                                            out_bf16);
+    }
   }
   return cudaGetLastError();
 }

@@ -66,6 +66,12 @@ cudaError_t launch_moe_gemm_tc(const GemmArgs& args, int bits, int cb, int block
 
 // Sum the P partials in part order, rotate, scale, store y, zero the workspace.
 cudaError_t launch_splitk_epilogue(const GemmArgs& args, cudaStream_t stream);
+// Weighted sum of each token's top-k rows of a grouped GEMM's output (pair_rows:
+// int32 [tokens * topk] scratch, rewritten by the call, never needs clearing).
+cudaError_t launch_moe_combine(const void* y, bool y_bf16, int64_t rows, int64_t n, const int32_t* sorted_ids,
+                               const int32_t* block_expert, int32_t block, int num_experts, const float* weights,
+                               int64_t num_tokens, int32_t topk, int32_t* pair_rows, void* out, bool out_bf16,
+                               cudaStream_t stream);
 
 cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream);
 cudaError_t launch_test_unpack(const int16_t* trellis, int bits, int cb, int64_t k, int64_t n, uint16_t* wq,

@@ -199,6 +199,36 @@ exl3_status_t exl3_moe_gemm(const uint16_t* xh, int64_t rows, int64_t k, const i
                             void* stream);
 
 /*
+ * exl3_moe_combine: the weighted sum of each token's top-k expert rows, the
+ * step after the grouped GEMM (the pages leave it to the caller: cuda-exl3
+ * README, "MoE notes"; the routing layout is the one above).
+ *   out[t, :] = sum over s = 0 .. topk-1, in that order, of
+ *               weights[t, s] * y[row(t, s), :]
+ * where row(t, s) is the padded row of a live block (expert id in
+ * [0, num_experts)) whose sorted_ids entry is the pair t * topk + s; a pair
+ * with no such row adds nothing (a token with none gets zeros).  The sum is
+ * fp32, one fused multiply-add per slot in slot order, then one rounding to
+ * out_dtype; padding rows and rows of blocks of no expert are never read.
+ *   y          device, [rows][n] of y_dtype (exl3_moe_gemm's output)
+ *   weights    device, fp32 [num_tokens][topk] (the router's top-k weights)
+ *   pair_rows  device, int32 [num_tokens * topk] scratch owned by the caller:
+ *              the call writes the row of every routed pair into it first and
+ *              checks each entry it reads against sorted_ids and block_expert,
+ *              so it needs no clearing between calls
+ *   out        device, [num_tokens][n] of out_dtype (output)
+ * Each pair must appear in at most one row of a live block (the layout above
+ * guarantees it; with duplicates the row taken is unspecified).  Two kernel
+ * launches on `stream`, no synchronisation, no allocation.  EXL3_EINVAL for
+ * sizes out of range, rows not a multiple of block, a block size other than
+ * 16, 32 or 128, topk outside 1..64, no experts, or a missing or misaligned
+ * pointer; num_tokens == 0 does nothing.
+ */
+exl3_status_t exl3_moe_combine(const void* y, exl3_dtype_t y_dtype, int64_t rows, int64_t n,
+                               const int32_t* sorted_ids, const int32_t* block_expert, int32_t block,
+                               int32_t num_experts, const float* weights, int64_t num_tokens, int32_t topk,
+                               int32_t* pair_rows, void* out, exl3_dtype_t out_dtype, void* stream);
+
+/*
  * exl3_gemm_splitk_noalloc -- the split-k GEMM for callers that cannot allocate.
  *
  * The pages have no counterpart to this call; it exists for callers that have

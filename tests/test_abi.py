@@ -132,6 +132,26 @@ def test_moe_entry_points_reject_invalid(L):
     assert L.exl3_moe_gemm(v, 24, 256, v, 4, 1, v, cols, 1, v, 16, 4, v, 1, 256, None) == 1  # 24 rows: not whole blocks
 
 
+def test_moe_combine_rejects_invalid(L):
+    v = ctypes.c_void_p(FAKE)
+    odd = ctypes.c_void_p(FAKE + 4)
+
+    def call(y=v, rows=64, n=256, block=32, experts=4, w=v, tokens=8, topk=2, pair_rows=v, out=v, out_dtype=1):
+        return L.exl3_moe_combine(y, 1, rows, n, v, v, block, experts, w, tokens, topk, pair_rows, out, out_dtype,
+                                  None)
+
+    assert call(block=64) == 1  # block size
+    assert call(rows=40) == 1  # rows not whole blocks
+    assert call(n=200) == 1  # n not a multiple of 128
+    assert call(topk=0) == 1 and call(topk=65) == 1
+    assert call(experts=0) == 1
+    assert call(out_dtype=2) == 1
+    assert call(pair_rows=None) == 1  # no scratch table
+    assert call(w=None) == 1  # no weights
+    assert call(out=odd) == 1 and call(y=odd) == 1  # misaligned
+    assert call(tokens=0, pair_rows=None, out=None, w=None) == 0  # no tokens: nothing to do
+
+
 def test_test_entry_points_reject_invalid(L):
     v = ctypes.c_void_p(FAKE)
     assert L.exl3_test_codebook(7, v, None) == 1

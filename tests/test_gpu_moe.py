@@ -109,3 +109,102 @@ def test_moe_rejections():
     xh = E.moe_input_transform(x.to(DEV), r.sorted_ids.to(DEV), 2, r.block_expert.to(DEV), 32, layer.suh.to(DEV))
     with pytest.raises(E.Exl3Error):  # block size 64 is not supported
         E.moe_gemm(xh, layer.trellis.to(DEV), 4, 1, layer.svh.to(DEV), layer.shard_cols, r.block_expert.to(DEV), 64)
+
+
+# ---------------------------------------------------------------------------
+# The weighted combine of each token's top-k rows (exl3_moe_combine)
+# ---------------------------------------------------------------------------
+
+COMBINE_CASES = [CASES[0], CASES[1], CASES[3], CASES[6]]
+BF16_NAN = 0x7FC1  # a bf16 NaN pattern: rows of skipped blocks keep it, so reading one would show
+
+
+def _routed_rows(layer, r, x, tokens, topk, block, block_expert):
+    """The grouped GEMM's output on the GPU, skipped blocks' rows left as NaN."""
+    tr, suh, svh = layer.trellis.to(DEV), layer.suh.to(DEV), layer.svh.to(DEV)
+    ids, be = r.sorted_ids.to(DEV), block_expert.to(DEV)
+    xh = E.moe_input_transform(x.to(DEV), ids, topk, be, block, suh)
+    y = torch.full((r.rows, layer.n), BF16_NAN, dtype=torch.int16, device=DEV).view(torch.bfloat16)
+    E.moe_gemm(xh, tr, layer.bits, layer.codebook, svh, layer.shard_cols, be, block, out=y)
+    return y, ids, be
+
+
+@pytest.mark.parametrize("case", COMBINE_CASES, ids=[f"t{c[0]}e{c[1]}k{c[2]}b{c[3]}" for c in COMBINE_CASES])
+@pytest.mark.parametrize("drop", [False, True], ids=["all", "dropped_block"])
+def test_moe_combine_against_oracle(case, drop):
+    """The whole routed layer plus combine against the oracle.  Each routed row
+    meets the per-column bar on its own; the combine's weights sum to 1, so the
+    error of a token is at most the weighted sum of its rows' bars plus the
+    final bf16 rounding (2^-8 relative, with margin for fp32 sums)."""
+    tokens, experts, topk, block, k, widths, bits, cb = case
+    layer, r, x = _setup(*case, seed=7300 + tokens)
+    be_host = r.block_expert.clone()
+    if drop:  # a live block marked as no expert: its pairs' terms disappear
+        be_host[int(torch.nonzero(be_host >= 0)[0])] = -1
+    y, ids, be = _routed_rows(layer, r, x, tokens, topk, block, be_host)
+    w = synthetic.make_topk_weights(tokens, topk, seed=7301 + tokens)
+    out = E.moe_combine(y, ids, be, block, experts, w.to(DEV), topk)
+    torch.cuda.synchronize()
+    rows = O.moe_linear(_np(x), r.sorted_ids.numpy(), be_host.numpy(), block, topk, layer.trellis.numpy(), bits, cb,
+                        _np(layer.suh), _np(layer.svh), layer.shard_cols)
+    ref = O.moe_combine(rows, r.sorted_ids.numpy(), be_host.numpy(), block, topk, w.double().numpy(), tokens,
+                        experts)
+    got = _np(out)
+    assert np.isfinite(got).all(), "a padding row or a skipped block's row was read"
+    colmax = np.nanmax(np.abs(rows), axis=0)  # each routed row's per-column bar is TOL * colmax
+    wsum = np.zeros(tokens)
+    ids_np = r.sorted_ids.numpy()
+    live = np.repeat(be_host.numpy() >= 0, block)
+    for row, pair in enumerate(ids_np):
+        if live[row] and pair < tokens * topk:
+            t, j = divmod(int(pair), topk)
+            wsum[t] += float(w[t, j])
+    bound = TOL * wsum[:, None] * colmax[None, :] + 2.0 ** -8 * np.abs(ref) + 1e-6
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), f"worst error / bound {np.max(err / bound):.3f}"
+    if drop:
+        assert (wsum < 1 - 1e-6).any(), "the dropped block held no routed pair"
+
+
+@pytest.mark.parametrize("case", COMBINE_CASES[:2], ids=[f"t{c[0]}e{c[1]}" for c in COMBINE_CASES[:2]])
+def test_moe_combine_one_hot_weights_return_the_slot_row(case):
+    """With weight 1 on slot j and 0 elsewhere, each token's output is its
+    slot-j row byte for byte (one fma with 1, zero terms add nothing, and the
+    rounding returns the bf16 value)."""
+    tokens, experts, topk, block, k, widths, bits, cb = case
+    layer, r, x = _setup(*case, seed=7400 + tokens)
+    y, ids, be = _routed_rows(layer, r, x, tokens, topk, block, r.block_expert)
+    ids_np = r.sorted_ids.numpy()
+    for j in range(topk):
+        w = torch.zeros((tokens, topk), dtype=torch.float32)
+        w[:, j] = 1.0
+        out = E.moe_combine(y, ids, be, block, experts, w.to(DEV), topk)
+        torch.cuda.synchronize()
+        rows = [int(np.nonzero(ids_np == t * topk + j)[0][0]) for t in range(tokens)]
+        assert torch.equal(out.view(torch.int16), y[rows].view(torch.int16))
+
+
+def test_moe_combine_scratch_needs_no_clearing():
+    """Any contents of the pair-row table before the call (garbage, or rows of
+    another routing) give the same bytes as a fresh table."""
+    case = CASES[1]
+    tokens, experts, topk, block, k, widths, bits, cb = case
+    layer, r, x = _setup(*case, seed=7500)
+    y, ids, be = _routed_rows(layer, r, x, tokens, topk, block, r.block_expert)
+    w = synthetic.make_topk_weights(tokens, topk, seed=7501).to(DEV)
+    want = E.moe_combine(y, ids, be, block, experts, w, topk)
+    g = torch.Generator().manual_seed(7502)
+    for lo, hi in ((-5, r.rows + 5), (0, r.rows)):
+        junk = torch.randint(lo, hi, (tokens * topk,), generator=g, dtype=torch.int32).to(DEV)
+        got = E.moe_combine(y, ids, be, block, experts, w, topk, pair_rows=junk)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+    # a table left by another routing of the same tokens
+    r2 = synthetic.make_routing(tokens, experts, topk, block, seed=7503)
+    table = torch.empty(tokens * topk, dtype=torch.int32, device=DEV)
+    E.moe_combine(y[:r2.rows] if r2.rows <= r.rows else y, r2.sorted_ids.to(DEV)[:min(r2.rows, r.rows)],
+                  r2.block_expert.to(DEV)[:min(r2.rows, r.rows) // block], block, experts, w, topk,
+                  pair_rows=table)
+    got = E.moe_combine(y, ids, be, block, experts, w, topk, pair_rows=table)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
