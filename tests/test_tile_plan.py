@@ -71,3 +71,34 @@ def test_plan_rejects_invalid():
         B.test_tile_plan(16, 5000, 12288, [0, 12288])
     with pytest.raises(B.Exl3Error):
         B.test_tile_plan(16, 5120, 12288, [0, 100, 12288])
+
+
+TAIL_BN = {N128: 128, N128R2: 128, N256R2: 256, N128R2P: 128, N64K4: 64, N32K4: 32}
+
+
+@pytest.mark.parametrize("k", [2048, 2176, 5120], ids=["k2048", "k2176_odd_blocks", "k5120"])
+@pytest.mark.parametrize("split_shards", [False, True], ids=["one_shard", "two_shards"])
+def test_split_plans_hold_over_a_grid(k, split_shards):
+    """Every split plan over a grid of widths and batch sizes: the first launch
+    is whole waves, the second covers exactly the pair tiles left, its tiles
+    divide the split-off columns and every shard edge, and four-atom strips only
+    appear when k holds an even number of 128-row blocks."""
+    checked = 0
+    for n in range(2048, 40961, 1024):
+        cols = [0, n // 2 // 128 * 128, n] if split_shards else [0, n]
+        for m in range(520, 8193, 184):
+            shape, tail, primary, row_base, col_base = plan(m, k, n, cols)
+            if tail < 0:
+                continue
+            bn = PAIR_BN[shape]
+            ncol, nrp = n // bn, -(-m // 512)
+            assert (2 * primary) % SMS == 0
+            assert row_base == (nrp - 1) * 512
+            assert (n - col_base) // bn == ncol * nrp - primary
+            tb = TAIL_BN[tail]
+            assert (n - col_base) % tb == 0 and col_base % 128 == 0
+            assert all(c % max(tb, 128) == 0 for c in cols), (n, m, tail, cols)
+            if tail in (N64K4, N32K4):
+                assert (k // 128) % 2 == 0
+            checked += 1
+    assert checked > 20
