@@ -31,6 +31,8 @@ def test_q_proj_plan(m, want):
 @pytest.mark.parametrize("m,k,n,cols,want", [
     (64, 12288, 4096, None, N32K4), (100, 12288, 4096, None, N32K4),  # 32 blocks: 128 strips of 32 columns
     (64, 4096, 8192, None, N64M64K4), (100, 4096, 8192, None, N64K4),  # 64 blocks: 64-column strips, four atoms
+    (64, 12416, 4096, None, N128), (100, 12416, 4096, None, N128),  # odd k/128: no four-atom strips
+    (64, 4096, 2048, None, N32K4),  # 16 blocks: 64 strips of 32 columns
     (128, 5120, 6144, None, N64K4), (100, 5120, 12288, None, N96),
     (48, 5120, 34816, [0, 17408, 34816], N256R2), (128, 4096, 154880, None, N256R2),  # wide: 256-column tiles
 ])
