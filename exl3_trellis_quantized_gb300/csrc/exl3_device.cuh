@@ -89,6 +89,48 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t s0, uint32_t s1) {
   }
 }
 
+// The same two values with the integer work spread over the ALU, multiply and
+// fp16 pipes (identical results, pinned against decode_pair over all states by
+// the codebook test).  mcg / 3inst: after the hash and mask, each value's two
+// halves are added by one fp16 fma per value, fma(hi, 1, lo) = lo + hi rounded
+// once, whose other lane computes hi * -1 + hi = +0 exactly, so the two partial
+// words {v0, +0} and {+0, v1} merge with one exact fp16 add instead of two byte
+// permutes.  mul1: the two biased byte sums merge with a multiply-add by 2^16
+// (each is below 2^16) instead of a byte permute.
+template <int CB>
+__device__ __forceinline__ uint32_t decode_pair_balanced(uint32_t s0, uint32_t s1, const DecodeConsts& mc) {
+  if constexpr (CB == CB_MUL1) {
+    const uint32_t u0 = s0 * kMul1Mult;
+    const uint32_t u1 = s1 * kMul1Mult;
+    const uint32_t t0 = __dp4a(u0, 0x01010101u, 0x6400u);
+    const uint32_t t1 = __dp4a(u1, 0x01010101u, 0x6400u);
+    uint32_t pk;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(pk) : "r"(t1), "r"(mc.pow2[16]), "r"(t0));
+    const uint32_t t = hsub2_u32(pk, kH2_1024);     // {t0, t1}, exact
+    return hfma2_u32(t, kMul1ScaleH2, kMul1BiasH2);  // one rounding each
+  } else {
+    uint32_t u0, u1;
+    if constexpr (CB == CB_3INST) {
+      u0 = s0 * k3instMult + k3instAdd;
+      u1 = s1 * k3instMult + k3instAdd;
+    } else {
+      u0 = s0 * kMcgMult;
+      u1 = s1 * kMcgMult;
+    }
+    u0 = lop3_mask_xor(u0);
+    u1 = lop3_mask_xor(u1);
+    const __half2 h0 = *reinterpret_cast<const __half2*>(&u0);
+    const __half2 h1 = *reinterpret_cast<const __half2*>(&u1);
+    const uint32_t k1u = 0xBC003C00u, k2u = 0x3C00BC00u;  // {1, -1}, {-1, 1}
+    const __half2 k1 = *reinterpret_cast<const __half2*>(&k1u);
+    const __half2 k2 = *reinterpret_cast<const __half2*>(&k2u);
+    const __half2 t0 = __hfma2(__high2half2(h0), k1, h0);  // {lo0 + hi0, +0}
+    const __half2 t1 = __hfma2(__low2half2(h1), k2, h1);   // {+0, lo1 + hi1}
+    const __half2 r = __hadd2(t0, t1);                     // {v0, v1}, exact
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Trellis windows.
 //

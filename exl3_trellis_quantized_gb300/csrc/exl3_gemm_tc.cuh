@@ -25,9 +25,10 @@
 // Warp roles:
 //   warp 0      trellis producer: one 3-D tensor copy per stage of the CTA's
 //               tiles for the stage's k16 rows;
-//   warp 1      TMEM allocator and MMA issuer: one thread issues tcgen05.mma
-//               kind::f16 (M=128, N=BN, K=16) per row group and k16 step, fp32
-//               accumulators in tensor memory;
+//   warp 1      TMEM allocator and MMA issuer: the warp runs the loop and
+//               one elected lane issues tcgen05.mma kind::f16 (M=128, N=BN,
+//               K=16) per row group and k16 step, fp32 accumulators in tensor
+//               memory (with SWAP, M=128 weight columns and N=XR rows);
 //   warp 2      activation producer: one 4-D tensor copy of xh (KA atoms,
 //               128-byte swizzle) per row group and stage;
 //   warp 3      with PAIR = 2, sends the CTA's decoded half of each stage to
@@ -51,6 +52,7 @@
 #pragma once
 
 #include "exl3_device.cuh"
+#include "exl3_gemm_tm.cuh"
 #include "exl3_launch.h"
 #include "exl3_sm100.cuh"
 
@@ -63,7 +65,12 @@ constexpr int kTcSmemBudget = 227 * 1024;
 
 constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 
-template <int BITS, int BN, int RG, int KA, int XR, int PAIR>
+// SWAP: the decoded weights are the tensor core's A operand (M = 128 weight
+// columns per instruction, the CTA's BN columns in its first rows) and the XR
+// activation rows its B operand (N = XR), so a small batch costs the tensor
+// core XR rows instead of 128.  The accumulator then holds one weight column
+// per tensor-memory lane and one batch row per tensor-memory column.
+template <int BITS, int BN, int RG, int KA, int XR, int PAIR, bool SWAP = false>
 struct TcCfg {
   static constexpr int kClusterX = 128 / gcd_int(BN, 128);  // CTAs spanning whole Hadamard blocks
   static constexpr int kCluster = kClusterX * PAIR;
@@ -91,8 +98,10 @@ struct TcCfg {
   static constexpr int kTRing = kWRing + kNW * kWSlot;
   static constexpr int kRingBytes = kTRing + kNT * kTSlot;
   static constexpr int kSmem = 1024 + kCtrlBytes + kRingBytes;
+  static constexpr int kMmaHalves = (BN + 127) / 128;  // SWAP: M = 128 instructions per k16 step
+  static constexpr int kAccCols = SWAP ? kMmaHalves * XR : RG * BN;
   static constexpr int kTmemCols =
-      RG * BN <= 32 ? 32 : RG * BN <= 64 ? 64 : RG * BN <= 128 ? 128 : RG * BN <= 256 ? 256 : 512;
+      kAccCols <= 32 ? 32 : kAccCols <= 64 ? 64 : kAccCols <= 128 ? 128 : kAccCols <= 256 ? 256 : 512;
   static constexpr int kTiles = kTrRows * (kBNL / 16);  // tiles decoded per stage
   static constexpr int kTpw = kTiles / kTcDecodeWarps;  // per decoder warp
   static constexpr int kZStride = BN + 4;               // epilogue staging row stride (floats)
@@ -105,8 +114,12 @@ struct TcCfg {
   static_assert(kTiles % kTcDecodeWarps == 0 && kTpw >= 1, "tiles per stage must split evenly over the decoders");
   static_assert(XR == 128 || RG == 1, "partial activation regions need a single row group");
   static_assert(kXSlot % 1024 == 0 && kWSlot % 1024 == 0, "operand slots must keep 1024-byte swizzle alignment");
-  static_assert(XR == 128 || kWRing - kXAtom + 16384 <= kRingBytes,
+  static_assert(SWAP || XR == 128 || kWRing - kXAtom + 16384 <= kRingBytes,
                 "the tensor core's 128-row read of the last atom must stay inside the rings");
+  static_assert(!SWAP || BN % 128 == 0 || kWRing + kNW * kWSlot - kWAtom + 16384 <= kRingBytes,
+                "the tensor core's 128-row read of the last weight atom must stay inside the rings");
+  static_assert(!SWAP || (RG == 1 && PAIR == 1 && XR % 16 == 0 && XR <= 64 && BN % 32 == 0),
+                "swapped operands: one row group of 16 to 64 rows, no pairs, whole 32-column quarters");
   static_assert(PAIR == 1 || (BN >= 128 && XR == 128), "pairs share whole 128-column blocks of full row groups");
   static_assert(kWHalfAtom % 1024 == 0, "each CTA's half of an atom must be whole 8-row swizzle groups");
   static_assert(128 * kZStride * 4 <= kRingBytes, "epilogue tile must fit in the rings");
@@ -117,15 +130,16 @@ struct TcCfg {
 // group), each with its own expert: blockIdx.y is the block,
 // a.block_expert[block] the expert (the trellis map then has the experts as a
 // fourth dimension and svh is [E][n]).
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool MOE = false>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool MOE = false, bool SWAP = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
-  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
+  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR, SWAP>;
   constexpr int NT = C::kNT;
   constexpr int NX = C::kNX;
   constexpr int NW = C::kNW;
   constexpr int CLX = C::kClusterX;
-  constexpr uint32_t kIdesc = idesc_f16_f32(128, BN);
+  constexpr uint32_t kIdesc = SWAP ? idesc_f16_f32(128, XR) : idesc_f16_f32(128, BN);
+  static_assert(!(SWAP && MOE), "the grouped GEMM keeps the activations as the A operand");
   const GemmArgs& a = p.a;
   static_assert(!MOE || (RG == 1 && PAIR == 1 && (BN == 128 || BN == 96)),
                 "grouped GEMM: one row group per block, 128 columns or 96-column strips");
@@ -288,14 +302,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // The whole warp runs the loop and one elected lane issues (see elect_one).
+    {
+      const uint32_t leader = elect_one();
       bool ok = true;
       int xs = 0, ws = 0;
       uint32_t xph = 0, wph = 0;
       const uint64_t xdesc0 = sdesc_sw128(smem_u32(rings + C::kXRing));
       const uint64_t wdesc0 = sdesc_sw128(smem_u32(rings + C::kWRing));
       for (int it = 0; it < nk; ++it) {
-        ok = mbar_wait(&xfull[xs], xph) && mbar_wait(&wfull[ws], wph);
+        // every lane waits; the vote keeps the warp's decision uniform
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(&xfull[xs], xph) && mbar_wait(&wfull[ws], wph));
         if (!ok) break;
         tc_fence_after();
         // descriptors of this stage's operands; an operand at byte offset o
@@ -306,19 +323,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int at = 0; at < KA; ++at) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            if constexpr (SWAP) {
+              // A: 128 decoded weight rows (columns of W) from the atom, B: the XR activation rows
 #pragma unroll
-            for (int r = 0; r < RG; ++r) {
-              tc_mma_f16(tmem + r * BN, dx + (uint64_t)((((r * KA + at) * C::kXAtom) + j * 32) >> 4),
-                         dwb + (uint64_t)((at * C::kWAtom + j * 32) >> 4), kIdesc, (it | at | j) != 0);
+              for (int h = 0; h < C::kMmaHalves; ++h) {
+                if (leader)
+                  tc_mma_f16(tmem + h * XR, dwb + (uint64_t)((at * C::kWAtom + h * 16384 + j * 32) >> 4),
+                             dx + (uint64_t)((at * C::kXAtom + j * 32) >> 4), kIdesc, (it | at | j) != 0);
+                __syncwarp();
+              }
+            } else {
+#pragma unroll
+              for (int r = 0; r < RG; ++r) {
+                if (leader)
+                  tc_mma_f16(tmem + r * BN, dx + (uint64_t)((((r * KA + at) * C::kXAtom) + j * 32) >> 4),
+                             dwb + (uint64_t)((at * C::kWAtom + j * 32) >> 4), kIdesc, (it | at | j) != 0);
+                __syncwarp();
+              }
             }
           }
         }
-        tc_commit(&xempty[xs]);
-        if (PAIR > 1) {
-          tc_commit_multicast(&wempty[ws], (uint16_t)3u);
-        } else {
-          tc_commit(&wempty[ws]);
+        if (leader) {
+          tc_commit(&xempty[xs]);
+          if (PAIR > 1) {
+            tc_commit_multicast(&wempty[ws], (uint16_t)3u);
+          } else {
+            tc_commit(&wempty[ws]);
+          }
         }
+        __syncwarp();
         if (++xs == NX) {
           xs = 0;
           xph ^= 1u;
@@ -328,8 +361,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wph ^= 1u;
         }
       }
-      if (!ok) *failed = 1u;
-      tc_commit(accfull);
+      if (leader) {
+        if (!ok) *failed = 1u;
+        tc_commit(accfull);
+      }
     }
     __syncwarp();
   } else {
@@ -372,39 +407,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* const wready = PAIR > 1 ? wdone : wfull;
     int ts = 0, ws = 0;
     uint32_t tph = 0, wph = 0;
+    constexpr int kStep = kTcDecodeWarps * kTileBytes;  // tiles of one warp are kTcDecodeWarps apart
     for (int it = 0; it < nk; ++it) {
       if (!mbar_wait(&tfull[ts], tph)) break;
       const uint32_t trbase = tring_u32 + (uint32_t)(ts * C::kTSlot);
-      // all window words of this warp's tiles first, so their latency overlaps
-      uint32_t wv[C::kTpw][3];
-#pragma unroll
-      for (int i = 0; i < C::kTpw; ++i) {
-        constexpr int kStep = kTcDecodeWarps * kTileBytes;  // tiles of one warp are kTcDecodeWarps apart
-        wv[i][0] = ld_shared_u32(trbase + word_off[0] + i * kStep);
-        wv[i][1] = ld_shared_u32(trbase + word_off[1] + i * kStep);
-        wv[i][2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2] + i * kStep) : 0u;
-      }
       const uint32_t wbase = wring_u32 + (uint32_t)(ws * C::kWSlot);
-      if constexpr (C::kDecodeFirst) {
-        // decode into registers first, so that waiting for the decoded-operand
-        // slot (consumed by the MMA(s) of its last use) overlaps the arithmetic
-        uint32_t b[C::kTpw][4];
+      if constexpr (XR < 128) {
+        // Small batches: one tile at a time, the next tile's window words
+        // loaded before this tile's decode and its store right after it.
+        // Every decoder warp starts a stage at about the same time: loading
+        // a whole stage's words first and storing all of its tiles last
+        // queued them on the shared-memory pipe in two bursts that left the
+        // warps waiting (measured 4-6% slower on 128-column tiles).
+        if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+        uint32_t wn[3];
+        wn[0] = ld_shared_u32(trbase + word_off[0]);
+        wn[1] = ld_shared_u32(trbase + word_off[1]);
+        wn[2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2]) : 0u;
 #pragma unroll
         for (int i = 0; i < C::kTpw; ++i) {
-          const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
-          decode_lane<BITS, CB>(al, mc, b[i]);
-        }
-        if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
-#pragma unroll
-        for (int i = 0; i < C::kTpw; ++i) stmatrix_x4(wbase + w_off[i], b[i][0], b[i][1], b[i][2], b[i][3]);
-      } else {
-        if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
-#pragma unroll
-        for (int i = 0; i < C::kTpw; ++i) {
-          const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
+          const uint32_t w0 = wn[0], w1 = wn[1], w2 = wn[2];
+          if (i + 1 < C::kTpw) {
+            const uint32_t o = (uint32_t)((i + 1) * kStep);
+            wn[0] = ld_shared_u32(trbase + word_off[0] + o);
+            wn[1] = ld_shared_u32(trbase + word_off[1] + o);
+            wn[2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2] + o) : 0u;
+          }
+          const Aligned al = align_window<BITS>(w0, w1, w2, lw.off);
           uint32_t b[4];
           decode_lane<BITS, CB>(al, mc, b);
           stmatrix_x4(wbase + w_off[i], b[0], b[1], b[2], b[3]);
+        }
+      } else {
+        // all window words of this warp's tiles first, so their latency overlaps
+        uint32_t wv[C::kTpw][3];
+#pragma unroll
+        for (int i = 0; i < C::kTpw; ++i) {
+          wv[i][0] = ld_shared_u32(trbase + word_off[0] + i * kStep);
+          wv[i][1] = ld_shared_u32(trbase + word_off[1] + i * kStep);
+          wv[i][2] = (LaneWindow<BITS>::kNeed == 3) ? ld_shared_u32(trbase + word_off[2] + i * kStep) : 0u;
+        }
+        if constexpr (C::kDecodeFirst) {
+          // decode into registers first, so that waiting for the decoded-operand
+          // slot (consumed by the MMA(s) of its last use) overlaps the arithmetic
+          uint32_t b[C::kTpw][4];
+#pragma unroll
+          for (int i = 0; i < C::kTpw; ++i) {
+            const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
+            decode_lane<BITS, CB>(al, mc, b[i]);
+          }
+          if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+#pragma unroll
+          for (int i = 0; i < C::kTpw; ++i) stmatrix_x4(wbase + w_off[i], b[i][0], b[i][1], b[i][2], b[i][3]);
+        } else {
+          if (!mbar_wait(&wempty[ws], wph ^ 1u)) break;
+#pragma unroll
+          for (int i = 0; i < C::kTpw; ++i) {
+            const Aligned al = align_window<BITS>(wv[i][0], wv[i][1], wv[i][2], lw.off);
+            uint32_t b[4];
+            decode_lane<BITS, CB>(al, mc, b);
+            stmatrix_x4(wbase + w_off[i], b[0], b[1], b[2], b[3]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -446,7 +509,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr bool kPackedRows = C::kClusterX == 1;
   float svf[kSpanBlocks][4];  // one column per lane and quarter
   uint2 svw[kSpanBlocks][4];  // four adjacent columns per lane and quarter, fp16 packed
-  if (warp >= kTcFirstDecoder && a.parts == 1) {
+  uint2 svs[kSpanBlocks];  // SWAP: columns 4l..4l+3 of each 128-column block of the span, fp16 packed
+  if (SWAP && warp >= kTcFirstDecoder && a.parts == 1) {
+#pragma unroll
+    for (int hb = 0; hb < kSpanBlocks; ++hb) svs[hb] = *reinterpret_cast<const uint2*>(svh + cbase + hb * 128 + 4 * lane);
+  }
+  if (!SWAP && warp >= kTcFirstDecoder && a.parts == 1) {
 #pragma unroll
     for (int hb = 0; hb < kSpanBlocks; ++hb)
 #pragma unroll
@@ -482,166 +550,234 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* zs = reinterpret_cast<float*>(rings);
   constexpr int kZ = C::kZStride;
 
-  if (a.parts > 1) {
-    // split-k: this part's fp32 sums go straight to acc[part][row][col]
-    if (warp >= kTcFirstDecoder) {
-      const int quarter = warp & 3;
-      float* dst = a.acc + (int64_t)part * a.m * a.n;
-      for (int r = 0; r < RG; ++r) {
-        for (int cc = dw >> 2; cc < BN / 32; cc += kTcDecodeWarps / 4) {
-          uint32_t q[32];
-          tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
-          tmem_ld_wait();
-          const int64_t row = row0 + r * 128 + quarter * 32 + lane;
-          if (ok && row < row_end) {
-            float4* o = reinterpret_cast<float4*>(dst + row * a.n + c0 + cc * 32);
+  if constexpr (SWAP) {
+    // Thread (quarter, h) of a decoder warp holds weight column h*128 +
+    // 32*quarter + lane of the CTA and its XR batch rows.
+    const int quarter = warp & 3;
+    const int h = dw >> 2;
+    const int col = h * 128 + quarter * 32 + lane;
+    const bool holds = warp >= kTcFirstDecoder && h < C::kMmaHalves && h * 128 + quarter * 32 < BN;
+    if (a.parts > 1) {
+      // split-k: this part's fp32 sums go straight to acc[part][row][col]
+      if (holds) {
+        uint32_t q[XR];
+        tmem_ld_32x32b_cols<XR>(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(h * XR), q);
+        tmem_ld_wait();
+        float* dst = a.acc + (int64_t)part * a.m * a.n + c0 + col;
+        if (ok) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              o[i] = make_float4(__uint_as_float(q[4 * i]), __uint_as_float(q[4 * i + 1]),
-                                 __uint_as_float(q[4 * i + 2]), __uint_as_float(q[4 * i + 3]));
-          }
+          for (int r = 0; r < XR; ++r)
+            if (row0 + r < row_end) dst[(row0 + r) * a.n] = __uint_as_float(q[r]);
+        }
+      }
+    } else {
+      // 1. tensor memory -> zs[row][col], raw fp32 sums
+      if (holds) {
+        uint32_t q[XR];
+        tmem_ld_32x32b_cols<XR>(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(h * XR), q);
+        tmem_ld_wait();
+#pragma unroll
+        for (int r = 0; r < XR; ++r) zs[r * kZ + col] = __uint_as_float(q[r]);
+      }
+      if (CLX > 1) {
+        cluster_sync();
+      } else {
+        __syncthreads();
+      }
+      // 2. one warp per (row, 128-column block of the span): lane l takes
+      // columns 4l..4l+3 (from whichever CTA of the cluster holds them), the
+      // full butterfly (strides 1, 2 in registers, 4..64 across lanes), scale
+      // and store four adjacent outputs.  The CTAs of a cluster split the rows.
+      if (warp >= kTcFirstDecoder) {
+        constexpr int kBlocks = CLX * BN / 128;
+        const int64_t live = row_end - row0 < XR ? row_end - row0 : XR;
+        for (int u = dw;; u += kTcDecodeWarps) {
+          const int rr = (int)rank + CLX * (u / kBlocks);
+          const int hb = u % kBlocks;
+          if (rr >= live) break;
+          const int span_col = hb * 128 + 4 * lane;
+          const uint32_t src_rank = (uint32_t)(span_col / BN);
+          const int local_col = span_col - (int)src_rank * BN;
+          const uint32_t zaddr = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) +
+                                 (uint32_t)((rr * kZ + local_col) * 4);
+          const float4 t = (CLX > 1) ? ld_shared_cluster_v4f(zaddr) : ld_shared_v4f(zaddr);
+          float v[4] = {t.x, t.y, t.z, t.w};
+          fwht128_warp(v, lane);
+          uint2 sv = svs[0];
+#pragma unroll
+          for (int i = 1; i < kSpanBlocks; ++i)
+            if (hb == i) sv = svs[i];
+          const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
+          const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+          const uint32_t o0 = f32_to_out((v[0] * 0.125f) * s01.x, bf16), o1 = f32_to_out((v[1] * 0.125f) * s01.y, bf16);
+          const uint32_t o2 = f32_to_out((v[2] * 0.125f) * s23.x, bf16), o3 = f32_to_out((v[3] * 0.125f) * s23.y, bf16);
+          if (ok)
+            *reinterpret_cast<uint2*>(y + (row0 + rr) * a.n + cbase + span_col) = make_uint2(o0 | (o1 << 16), o2 | (o3 << 16));
         }
       }
     }
   } else {
-    constexpr int kSpan = CLX * BN;  // whole 128-column blocks
-    for (int r = 0; r < RG; ++r) {
-      // 1. tensor memory -> zs[128][BN].  Each thread holds one row's 32
-      // consecutive columns after a load and runs the Hadamard stages of
-      // stride 1..16 on them in registers (those pairs never leave a 32-column
-      // chunk), so only the stride-32 and stride-64 stages remain.
+    if (a.parts > 1) {
+      // split-k: this part's fp32 sums go straight to acc[part][row][col]
       if (warp >= kTcFirstDecoder) {
         const int quarter = warp & 3;
-        const bool live = row0 + r * 128 + quarter * 32 < row_end;  // this quarter holds stored rows
-        for (int cc = dw >> 2; live && cc < BN / 32; cc += kTcDecodeWarps / 4) {
-          uint32_t q[32];
-          tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
-          tmem_ld_wait();
-          float v[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(q[e]);
-          fwht32_regs(v);
-          float* dst = zs + (quarter * 32 + lane) * kZ + cc * 32;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+        float* dst = a.acc + (int64_t)part * a.m * a.n;
+        for (int r = 0; r < RG; ++r) {
+          for (int cc = dw >> 2; cc < BN / 32; cc += kTcDecodeWarps / 4) {
+            uint32_t q[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
+            tmem_ld_wait();
+            const int64_t row = row0 + r * 128 + quarter * 32 + lane;
+            if (ok && row < row_end) {
+              float4* o = reinterpret_cast<float4*>(dst + row * a.n + c0 + cc * 32);
+  #pragma unroll
+              for (int i = 0; i < 8; ++i)
+                o[i] = make_float4(__uint_as_float(q[4 * i]), __uint_as_float(q[4 * i + 1]),
+                                   __uint_as_float(q[4 * i + 2]), __uint_as_float(q[4 * i + 3]));
+            }
+          }
         }
       }
-      if (CLX > 1) {
-        cluster_sync();
-      } else {
-        __syncthreads();
-      }
-      if constexpr (kPackedRows) {
-        // 2. rows: eight lanes per row, four rows per warp step.  Lane j of a
-        // row owns columns 4j..4j+3 of each 32-column quarter of a 128-column
-        // block of the span: the stride-32 and stride-64 stages, then scale and
-        // store four adjacent outputs (8 bytes) per quarter.
+    } else {
+      constexpr int kSpan = CLX * BN;  // whole 128-column blocks
+      for (int r = 0; r < RG; ++r) {
+        // 1. tensor memory -> zs[128][BN].  Each thread holds one row's 32
+        // consecutive columns after a load and runs the Hadamard stages of
+        // stride 1..16 on them in registers (those pairs never leave a 32-column
+        // chunk), so only the stride-32 and stride-64 stages remain.
         if (warp >= kTcFirstDecoder) {
-          const int j = lane & 7, sr = lane >> 3;
+          const int quarter = warp & 3;
+          const bool live = row0 + r * 128 + quarter * 32 < row_end;  // this quarter holds stored rows
+          for (int cc = dw >> 2; live && cc < BN / 32; cc += kTcDecodeWarps / 4) {
+            uint32_t q[32];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
+            tmem_ld_wait();
+            float v[32];
   #pragma unroll
-          for (int hb = 0; hb < kSpan / 128; ++hb) {
-            uint32_t zsrc[4];
-            int64_t col[4];
-            float sv[4][4];
+            for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(q[e]);
+            fwht32_regs(v);
+            float* dst = zs + (quarter * 32 + lane) * kZ + cc * 32;
   #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              // a quarter never straddles two CTAs: BN is a multiple of 32
-              const int span_col = hb * 128 + 32 * i + 4 * j;
-              const uint32_t src_rank = (uint32_t)(span_col / BN);
-              const int local_col = span_col - (int)src_rank * BN;
-              col[i] = cbase + span_col;
-              zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
-              const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].x));
-              const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].y));
-              sv[i][0] = s01.x;
-              sv[i][1] = s01.y;
-              sv[i][2] = s23.x;
-              sv[i][3] = s23.y;
-            }
-            for (int rb = (int)rank + CLX * 4 * dw; rb < 128; rb += CLX * 4 * kTcDecodeWarps) {
-              const int rr = rb + CLX * sr;  // < 128: rb + 3 * CLX stays inside the group
-              const int64_t row = row0 + r * 128 + rr;
-              float v[4][4];
-  #pragma unroll
+            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          }
+        }
+        if (CLX > 1) {
+          cluster_sync();
+        } else {
+          __syncthreads();
+        }
+        if constexpr (kPackedRows) {
+          // 2. rows: eight lanes per row, four rows per warp step.  Lane j of a
+          // row owns columns 4j..4j+3 of each 32-column quarter of a 128-column
+          // block of the span: the stride-32 and stride-64 stages, then scale and
+          // store four adjacent outputs (8 bytes) per quarter.
+          if (warp >= kTcFirstDecoder) {
+            const int j = lane & 7, sr = lane >> 3;
+    #pragma unroll
+            for (int hb = 0; hb < kSpan / 128; ++hb) {
+              uint32_t zsrc[4];
+              int64_t col[4];
+              float sv[4][4];
+    #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
-                const float4 t = (CLX > 1) ? ld_shared_cluster_v4f(addr) : ld_shared_v4f(addr);
-                v[i][0] = t.x;
-                v[i][1] = t.y;
-                v[i][2] = t.z;
-                v[i][3] = t.w;
+                // a quarter never straddles two CTAs: BN is a multiple of 32
+                const int span_col = hb * 128 + 32 * i + 4 * j;
+                const uint32_t src_rank = (uint32_t)(span_col / BN);
+                const int local_col = span_col - (int)src_rank * BN;
+                col[i] = cbase + span_col;
+                zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
+                const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].x));
+                const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&svw[hb][i].y));
+                sv[i][0] = s01.x;
+                sv[i][1] = s01.y;
+                sv[i][2] = s23.x;
+                sv[i][3] = s23.y;
               }
-              if (ok && row < row_end) {
-                uint16_t* yr = y + row * a.n;
-  #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
-                  const float a0 = v[0][e] + v[1][e], a1 = v[0][e] - v[1][e];
-                  const float a2 = v[2][e] + v[3][e], a3 = v[2][e] - v[3][e];
-                  v[0][e] = a0 + a2;
-                  v[2][e] = a0 - a2;
-                  v[1][e] = a1 + a3;
-                  v[3][e] = a1 - a3;
-                }
-  #pragma unroll
+              for (int rb = (int)rank + CLX * 4 * dw; rb < 128; rb += CLX * 4 * kTcDecodeWarps) {
+                const int rr = rb + CLX * sr;  // < 128: rb + 3 * CLX stays inside the group
+                const int64_t row = row0 + r * 128 + rr;
+                float v[4][4];
+    #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                  uint32_t o[4];
-  #pragma unroll
-                  for (int e = 0; e < 4; ++e) o[e] = f32_to_out((v[i][e] * 0.125f) * sv[i][e], bf16);
-                  *reinterpret_cast<uint2*>(yr + col[i]) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+                  const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
+                  const float4 t = (CLX > 1) ? ld_shared_cluster_v4f(addr) : ld_shared_v4f(addr);
+                  v[i][0] = t.x;
+                  v[i][1] = t.y;
+                  v[i][2] = t.z;
+                  v[i][3] = t.w;
+                }
+                if (ok && row < row_end) {
+                  uint16_t* yr = y + row * a.n;
+    #pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
+                    const float a0 = v[0][e] + v[1][e], a1 = v[0][e] - v[1][e];
+                    const float a2 = v[2][e] + v[3][e], a3 = v[2][e] - v[3][e];
+                    v[0][e] = a0 + a2;
+                    v[2][e] = a0 - a2;
+                    v[1][e] = a1 + a3;
+                    v[3][e] = a1 - a3;
+                  }
+    #pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    uint32_t o[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = f32_to_out((v[i][e] * 0.125f) * sv[i][e], bf16);
+                    *reinterpret_cast<uint2*>(yr + col[i]) = make_uint2(o[0] | (o[1] << 16), o[2] | (o[3] << 16));
+                  }
                 }
               }
             }
           }
-        }
-      } else {
-        // 2. rows: lane l owns columns l, l+32, l+64, l+96 of each 128-column
-        // block of the span: the stride-32 and stride-64 stages, then scale and
-        // store (each store instruction writes 32 consecutive columns)
-        if (warp >= kTcFirstDecoder) {
-  #pragma unroll
-          for (int hb = 0; hb < kSpan / 128; ++hb) {
-            uint32_t zsrc[4];
-            int64_t col[4];
-  #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int span_col = hb * 128 + lane + 32 * i;
-              const uint32_t src_rank = (uint32_t)(span_col / BN);
-              const int local_col = span_col - (int)src_rank * BN;
-              col[i] = cbase + span_col;
-              zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
-            }
-            for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
-              const int64_t row = row0 + r * 128 + rr;
-              if (!ok || row >= row_end) break;  // rows ascend with rr
-              float v[4];
-  #pragma unroll
+        } else {
+          // 2. rows: lane l owns columns l, l+32, l+64, l+96 of each 128-column
+          // block of the span: the stride-32 and stride-64 stages, then scale and
+          // store (each store instruction writes 32 consecutive columns)
+          if (warp >= kTcFirstDecoder) {
+    #pragma unroll
+            for (int hb = 0; hb < kSpan / 128; ++hb) {
+              uint32_t zsrc[4];
+              int64_t col[4];
+    #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
-                v[i] = (CLX > 1) ? ld_shared_cluster_f32(addr) : ld_shared_f32(addr);
+                const int span_col = hb * 128 + lane + 32 * i;
+                const uint32_t src_rank = (uint32_t)(span_col / BN);
+                const int local_col = span_col - (int)src_rank * BN;
+                col[i] = cbase + span_col;
+                zsrc[i] = ((CLX > 1) ? mapa_shared(smem_u32(zs), src_rank) : smem_u32(zs)) + (uint32_t)(local_col * 4);
               }
-              // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
-              const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-              v[0] = a0 + a2;
-              v[2] = a0 - a2;
-              v[1] = a1 + a3;
-              v[3] = a1 - a3;
-              uint16_t* yr = y + row * a.n;
-  #pragma unroll
-              for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[hb][i], bf16);
+              for (int rr = (int)rank + CLX * dw; rr < 128; rr += CLX * kTcDecodeWarps) {
+                const int64_t row = row0 + r * 128 + rr;
+                if (!ok || row >= row_end) break;  // rows ascend with rr
+                float v[4];
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const uint32_t addr = zsrc[i] + (uint32_t)(rr * kZ * 4);
+                  v[i] = (CLX > 1) ? ld_shared_cluster_f32(addr) : ld_shared_f32(addr);
+                }
+                // stride 32: (0,1), (2,3); stride 64: (0,2), (1,3)
+                const float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+                v[0] = a0 + a2;
+                v[2] = a0 - a2;
+                v[1] = a1 + a3;
+                v[3] = a1 - a3;
+                uint16_t* yr = y + row * a.n;
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) yr[col[i]] = f32_to_out((v[i] * 0.125f) * svf[hb][i], bf16);
+              }
             }
           }
         }
-      }
-      // the tile is reused by the next row group, and partners may still read it
-      if (CLX > 1) {
-        cluster_sync();
-      } else {
-        __syncthreads();
+        // the tile is reused by the next row group, and partners may still read it
+        if (CLX > 1) {
+          cluster_sync();
+        } else {
+          __syncthreads();
+        }
       }
     }
-  }
 
+  }
   tc_fence_before();
   if (C::kCluster > 1) {
     cluster_sync();
@@ -651,10 +787,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool MOE = false>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool MOE = false, bool SWAP = false>
 cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
-  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR>;
-  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, MOE>;
+  using C = TcCfg<BITS, BN, RG, KA, XR, PAIR, SWAP>;
+  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, MOE, SWAP>;
   // the shared-memory opt-in, once per device (benign race: every thread sets
   // the same attribute)
   static bool configured[64] = {};
@@ -711,6 +847,12 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN64M64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 64>(maps, p, stream);
     case TcShape::kN64K4: return launch_tc_variant<BITS, CB, 64, 1, 4, 128>(maps, p, stream);
     case TcShape::kN32K4: return launch_tc_variant<BITS, CB, 32, 1, 4, 128>(maps, p, stream);
+    case TcShape::kT128K4: return launch_tm_variant<BITS, CB, 4, 32>(maps, p, stream);
+    case TcShape::kT128: return launch_tm_variant<BITS, CB, 2, 32>(maps, p, stream);
+    case TcShape::kS96K4: return launch_tc_variant<BITS, CB, 96, 1, 4, 32, 1, false, true>(maps, p, stream);
+    case TcShape::kT128K4X16: return launch_tm_variant<BITS, CB, 4, 16>(maps, p, stream);
+    case TcShape::kS96K4X16: return launch_tc_variant<BITS, CB, 96, 1, 4, 16, 1, false, true>(maps, p, stream);
+    case TcShape::kT128X16: return launch_tm_variant<BITS, CB, 2, 16>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

@@ -193,15 +193,24 @@ cudaError_t launch_moe_combine(const void* y, bool y_bf16, int64_t rows, int64_t
 // Test-only kernels: the same device decode as the GEMM, written out densely.
 // ---------------------------------------------------------------------------
 template <int CB>
-__global__ void test_codebook_kernel(uint16_t* out) {
+__global__ void test_codebook_kernel(uint16_t* out, const DecodeConsts dc) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;  // states 2t, 2t+1
-  if (t < 32768) reinterpret_cast<uint32_t*>(out)[t] = decode_pair<CB>(2u * t, 2u * t + 1u);
+  if (t >= 32768) return;
+  // Both decoders of a state pair: the table holds their common value, or
+  // 0xFFFF (a NaN, which no state decodes to) where they disagree.
+  const uint32_t v = decode_pair<CB>(2u * t, 2u * t + 1u);
+  const uint32_t w = decode_pair_balanced<CB>(2u * t, 2u * t + 1u, dc);
+  const uint32_t lo = (v & 0xFFFFu) == (w & 0xFFFFu) ? (v & 0xFFFFu) : 0xFFFFu;
+  const uint32_t hi = (v >> 16) == (w >> 16) ? (v >> 16) : 0xFFFFu;
+  reinterpret_cast<uint32_t*>(out)[t] = lo | (hi << 16);
 }
 
 cudaError_t launch_test_codebook(int cb, uint16_t* out, cudaStream_t stream) {
-  if (cb == CB_3INST) test_codebook_kernel<CB_3INST><<<128, 256, 0, stream>>>(out);
-  else if (cb == CB_MCG) test_codebook_kernel<CB_MCG><<<128, 256, 0, stream>>>(out);
-  else test_codebook_kernel<CB_MUL1><<<128, 256, 0, stream>>>(out);
+  DecodeConsts dc;
+  fill_decode_consts(&dc);
+  if (cb == CB_3INST) test_codebook_kernel<CB_3INST><<<128, 256, 0, stream>>>(out, dc);
+  else if (cb == CB_MCG) test_codebook_kernel<CB_MCG><<<128, 256, 0, stream>>>(out, dc);
+  else test_codebook_kernel<CB_MUL1><<<128, 256, 0, stream>>>(out, dc);
   return cudaGetLastError();
 }
 

@@ -115,7 +115,16 @@ enum class TcShape : int {
   kN64K4,        // BN=64,  RG=1, KA=4, XR=128 (m <= 128, split-off tails; k/128 even, no split-k)
   kN32K4,        // BN=32,  RG=1, KA=4, XR=128 (m <= 128 on narrow layers, split-off tails; k/128 even,
                  //                             no split-k)
-  kLast = kN32K4,
+  // Decoded weights as the tensor core's A operand (M = 128 weight columns),
+  // the XR activation rows as B (N = XR): kT* keep A in tensor memory
+  // (exl3_gemm_tm.cuh), kS* in shared memory (strips in clusters of four).
+  kT128K4,       // BN=128, KA=4, XR=32 (m <= 32, k/128 even, no split-k)
+  kT128,         // BN=128, KA=2, XR=32 (m <= 32)
+  kS96K4,        // BN=96,  KA=4, XR=32 (m <= 32, k/128 even, no split-k, n and shard edges multiples of 384)
+  kT128K4X16,    // BN=128, KA=4, XR=16 (m <= 16, k/128 even, no split-k)
+  kS96K4X16,     // BN=96,  KA=4, XR=16 (m <= 16, k/128 even, no split-k, 384-aligned edges)
+  kT128X16,      // BN=128, KA=2, XR=16 (m <= 16)
+  kLast = kT128X16,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

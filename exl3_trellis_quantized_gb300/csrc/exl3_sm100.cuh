@@ -180,6 +180,37 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
       : "memory");
 }
+// 1 in one lane of the (converged) warp, 0 in the others.  The tensor-core
+// issue loops run on the whole warp, so their operand descriptors are computed
+// once per warp in uniform registers, and only the elected lane issues:
+// measured on GB300 at 16-18 cycles per tcgen05.mma under a full decoder load,
+// against 55-73 cycles for a loop run by lane 0 alone (whose descriptors go
+// from per-thread to uniform registers at every instruction) and 100-130 for
+// the whole warp issuing with a per-lane predicate.
+__device__ __forceinline__ uint32_t elect_one() {
+  uint32_t e;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(e));
+  return e;
+}
+// D[tmem] (+)= A[tmem] * B[smem]^T: A (M = 128 rows, one per lane; 16 fp16 of
+// k as 8 columns, k pairs low half first) read from tensor memory.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+      : "memory");
+}
+// 32 lanes x 8 consecutive 32-bit columns from registers: thread t writes lane t of its warp's quarter.
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), "r"(r[0]),
+      "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+// Wait until this thread's tensor-memory stores have completed.
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 // Arrive on the mbarrier once every tcgen05 op issued so far by this thread completes.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -206,6 +237,26 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// 32 lanes x N consecutive 32-bit columns (N a multiple of 16), in loads of
+// 32 and 16 columns.
+template <int N>
+__device__ __forceinline__ void tmem_ld_32x32b_cols(uint32_t taddr, uint32_t (&r)[N]) {
+  static_assert(N % 16 == 0, "whole 16-column loads");
+#pragma unroll
+  for (int c = 0; c + 32 <= N; c += 32)
+    tmem_ld_32x32b_x32(taddr + (uint32_t)c, *reinterpret_cast<uint32_t(*)[32]>(&r[c]));
+  if constexpr (N % 32 == 16) tmem_ld_32x32b_x16(taddr + (uint32_t)(N - 16), &r[N - 16]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

@@ -104,6 +104,12 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kN64M64K4: return {64, 4, 64, 1, 1};
     case TcShape::kN64K4: return {64, 4, 128, 1, 1};
     case TcShape::kN32K4: return {32, 4, 128, 1, 1};
+    case TcShape::kT128K4: return {128, 4, 32, 1, 1};
+    case TcShape::kT128: return {128, 2, 32, 1, 1};
+    case TcShape::kS96K4: return {96, 4, 32, 1, 1};
+    case TcShape::kT128K4X16: return {128, 4, 16, 1, 1};
+    case TcShape::kS96K4X16: return {96, 4, 16, 1, 1};
+    case TcShape::kT128X16: return {128, 2, 16, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -116,11 +122,18 @@ ShapeDims dims_of(TcShape s) {
 // 128-column CTA, measured on GB300 (q_proj-like layer, m = 1 to 32): narrow
 // strips spend more of each SM on the cluster, per-stage synchronisation and
 // the tensor core's 128-row operand reads.
-constexpr double kRel64 = 0.48, kRel32 = 0.43, kRel96 = 0.81;
-// More k per stage for the narrow strips (12288 x 4096 and 2048 x 4096, m = 1
-// to 32): 64-column strips on four atoms, 32-column strips on eight once k
-// holds eight or more such stages (fewer leave too short a pipeline).
-constexpr double kRel64K4 = 0.57, kRel32K8 = 0.48;
+constexpr double kRel96 = 0.81;
+// m <= 32, per CTA against a 128-column tensor-memory CTA (kT128*) in one
+// wave, measured on GB300 with the tensor-core instructions issued by an
+// elected lane (5120 x 12288, 5120 x 6144, 4096 x 8192, 12288 x 4096,
+// 2048 x 4096, m = 1 to 32): 96-column strips with the decoded weights as the
+// tensor core's 128-row operand, 64- and 32-column strips with two or four
+// (64) and four or eight (32) k atoms per stage.
+constexpr double kRel96S = 0.85, kRel64 = 0.52, kRel64K4 = 0.68, kRel32 = 0.50, kRel32K8 = 0.55;
+// The tensor-memory kernel is persistent: its per-CTA start and epilogue are
+// paid once per SM, not once per wave, so its rate per CTA grows with the
+// waves a layer needs (5120 x 34816: 2 waves, 4096 x 154880: 8 waves).
+double rel_tm(int64_t waves) { return waves <= 1 ? 1.02 : waves == 2 ? 1.06 : waves == 3 ? 1.15 : 1.3; }
 // 256-column, 256-row tiles at 32 < m <= 128 against 128 columns, per column
 // (5120 x 34816, 4096 x 154880): fewer CTAs in whole waves.
 constexpr double kRel256Mid = 1.07;
@@ -275,19 +288,22 @@ TcShape choose_shape(const GemmArgs& a) {
   }
   if (a.m <= 32) {
     // pick the column width whose grid keeps the most decode throughput busy
-    const double r128 = small_batch_rate(a.n / 128, 1.0);
-    const double r64 = small_batch_rate(a.n / 64, (a.k / 128) % 2 == 0 ? kRel64K4 : kRel64);
-    // 32-column strips take 4 k atoms per stage (k/128 even) or 8 (k a
-    // multiple of 512 and at least 4096); 64-column strips 4 when k/128 is even
+    const int64_t sms = sm_count();
+    const int64_t blocks = a.n / 128;
+    const double rt = rel_tm((blocks + sms - 1) / sms) * (double)(blocks < sms ? blocks : sms);
+    // four k atoms per stage halve the per-stage synchronisation (k must hold
+    // an even number of 128-blocks); 32-column strips take eight once k holds
+    // four or more such stages
     const bool k4 = (a.k / 128) % 2 == 0;
-    const bool k8 = a.k % 512 == 0 && a.k >= 4096;
+    const bool k8 = a.k % 512 == 0 && a.k >= 2048;
+    const double r64 = small_batch_rate(a.n / 64, k4 ? kRel64K4 : kRel64);
     const double r32 = k8 ? small_batch_rate(a.n / 32, kRel32K8) : k4 ? small_batch_rate(a.n / 32, kRel32) : 0.0;
     // 96-column strips: clusters of four over three Hadamard blocks
-    const double r96 = k4 && edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
-    // four k atoms per stage halve the per-stage synchronisation (k must hold
-    // an even number of 128-blocks)
-    if (r128 >= r96 && r128 >= r64 && r128 >= r32) return k4 ? TcShape::kN128SmallK4 : TcShape::kN128Small;
-    if (r96 >= r64 && r96 >= r32) return TcShape::kN96SmallK4;
+    const double r96 = k4 && edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96S) : 0.0;
+    const bool x16 = a.m <= 16;  // the 16-row tiles read half the activations
+    if (rt >= r96 && rt >= r64 && rt >= r32)
+      return k4 ? (x16 ? TcShape::kT128K4X16 : TcShape::kT128K4) : (x16 ? TcShape::kT128X16 : TcShape::kT128);
+    if (r96 >= r64 && r96 >= r32) return x16 ? TcShape::kS96K4X16 : TcShape::kS96K4;
     if (r64 >= r32) return k4 ? TcShape::kN64SmallK4 : TcShape::kN64Small;
     return k8 ? TcShape::kN32SmallK8 : TcShape::kN32Small;
   }

@@ -261,7 +261,9 @@ exl3_status_t exl3_gemm_splitk_noalloc(const uint16_t* xh, int64_t m, int64_t k,
  * Test-only entry points (they run the same device decode as exl3_gemm).
  *
  * exl3_test_codebook: out[s] = fp16 bits of codebook cb at state s, s = 0..65535
- *   (TensorFold PR #740, "Tests": all 65,536 states of each codebook).
+ *   (TensorFold PR #740, "Tests": all 65,536 states of each codebook).  The
+ *   library decodes with two instruction sequences (one per kernel family);
+ *   a state where they disagree reads 0xFFFF, a NaN no state decodes to.
  *   out: device, uint16 [65536].
  * exl3_test_unpack: wq[k][n] = decoded weights of the whole trellis as fp16 bits
  *   (TensorFold PR #740, "Tests": random tiles at every width and codebook).
@@ -298,10 +300,18 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
  *         four (m <= 64, k/128 even, no split-k), 16 = 64-column strips of
  *         128 rows with four (k/128 even, no split-k), 17 = 32-column strips
  *         of 128 rows with four (k/128 even, no split-k).
+ *     The decoded weights as the tensor core's 128-row operand and the batch
+ *     rows as the narrow one (18, 19, 21, 23 keep the decoded weights in
+ *     tensor memory, 20 and 22 in shared memory):
+ *     18 = 128 columns, four k atoms per stage (m <= 32, k/128 even, no
+ *         split-k), 19 = 128 columns, two k atoms (m <= 32), 20 = 96-column
+ *         strips in clusters of four, four k atoms (m <= 32, k/128 even, no
+ *         split-k, n and shard edges multiples of 384), 21 and 22 = 18 and 20
+ *         holding 16 rows (m <= 16), 23 = 19 holding 16 rows (m <= 16).
  * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
  * call (the conditions in parentheses).
  */
-#define EXL3_TEST_TILE_SHAPES 18
+#define EXL3_TEST_TILE_SHAPES 24
 exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
                                    const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                    const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,

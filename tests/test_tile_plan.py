@@ -8,7 +8,7 @@ from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
 (N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
- N64M64K4, N64K4, N32K4) = range(18)
+ N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16) = range(24)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -17,7 +17,9 @@ def plan(m, k, n, cols=None, split=False):
 
 
 @pytest.mark.parametrize("m,want", [
-    (1, (N96SK4, -1, 0, 0, 0)), (16, (N96SK4, -1, 0, 0, 0)),  # 96 column blocks: 96-column strips, 128 SMs
+    # 96 column blocks: 96-column strips on 128 SMs, the decoded weights as
+    # the tensor core's 128-row operand, 16-row tiles up to 16 rows
+    (1, (S96K4X16, -1, 0, 0, 0)), (16, (S96K4X16, -1, 0, 0, 0)), (32, (S96K4, -1, 0, 0, 0)),
     (48, (N96M64K4, -1, 0, 0, 0)), (64, (N96M64K4, -1, 0, 0, 0)),  # 64-row strips, four atoms a stage
     (128, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
     (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
@@ -42,8 +44,14 @@ def test_mid_batch_plan(m, k, n, cols, want):
 
 def test_narrow_and_split_layers():
     assert plan(16, 12288, 4096)[0] == N32SK8  # 32 column blocks: 32-column strips on 128 SMs, 8 atoms a stage
-    assert plan(16, 2048, 4096)[0] == N32S  # k = 2048: four atoms a stage keep the pipeline long enough
-    assert plan(16, 5120, 34816, [0, 17408, 34816])[0] == N128SK4  # 272 blocks fill the GPU at 128 columns
+    assert plan(16, 2048, 4096)[0] == N32SK8  # k = 2048 holds four stages of eight atoms
+    assert plan(32, 2048, 4096)[0] == N32SK8
+    # 272 blocks fill the GPU at 128 columns: the persistent tensor-memory kernel
+    assert plan(16, 5120, 34816, [0, 17408, 34816])[0] == T128K4X16
+    assert plan(32, 5120, 34816, [0, 17408, 34816])[0] == T128K4
+    assert plan(16, 4096, 154880)[0] == T128K4X16
+    assert plan(16, 4224, 154880)[0] == T128X16  # odd k/128: two atoms a stage
+    assert plan(16, 4096, 8192)[0] == N64SK4  # 64 blocks: 64-column strips, four atoms a stage
     assert plan(16, 384, 4096)[0] != N32S  # odd k/128: no four-atom tiles
     # split-k down projection: 7 parts of 40 blocks; 256-column CTAs need fewer waves
     assert plan(16, 17408, 5120, split=True)[0] == N256R2
