@@ -50,6 +50,24 @@ WORKLOADS = {
 }
 
 
+def weight_copies(k, n, bits):
+    """Copies of the weights the timed loops rotate over: enough that their total
+    exceeds 3x L2, so every launch reads its trellis from HBM."""
+    wbytes = k * n * bits // 8
+    return max(3, -(-3 * L2_BYTES // wbytes)), wbytes
+
+
+def workload_config(args, wl_name, world):
+    """The config dict of a workload's JSON line (the same for both arms)."""
+    desc, k, widths, bits, cb, ms, split = WORKLOADS[wl_name]
+    n = sum(widths)
+    copies, wbytes = weight_copies(k, n, bits)
+    return {"workload": desc, "k": k, "n": n, "bits": bits, "codebook": ["3inst", "mcg", "mul1"][cb],
+            "m": ms, "split_k": split, "parallelism": f"replicas x{world} (rows independent)",
+            "tile_shape": "autotuned in warm-up" if args.autotune else "cost model",
+            "l2": f"weights rotate over {copies} copies ({copies * wbytes / 1e6:.0f} MB > 3x L2)"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -186,8 +204,8 @@ def run_gpu(args, wl_name):
 
     layer = synthetic.make_layer(k, widths, bits, cb, seed=1002)
     n = layer.n
-    wbytes = layer.trellis.numel() * 2
-    copies = max(3, -(-3 * L2_BYTES // wbytes))
+    copies, wbytes = weight_copies(k, n, bits)
+    assert wbytes == layer.trellis.numel() * 2
     trs = [layer.trellis.to(dev)]
     for _ in range(copies - 1):
         trs.append(trs[0].clone())
@@ -219,23 +237,26 @@ def run_gpu(args, wl_name):
             E.gemm(xh[i], tr, bits, cb, svh, layer.shard_cols, out=ys[i])
 
     counter = [0]
-    # the dominant call: the largest batch, whose GEMM the roofline reports
+    # the dominant call: the largest batch, whose GEMM the roofline reports;
+    # the small call: m = 16 (else the smallest batch), the HBM-bound regime,
+    # reported as roofline_small
     dom = max(range(len(ms)), key=lambda i: ms[i])
+    small = ms.index(16) if 16 in ms else min(range(len(ms)), key=lambda i: ms[i])
 
     def step(events=None, gemm_events=None):
         for i in range(len(ms)):
             if events is not None:
                 events[i][0].record(stream)
-            if gemm_events is not None and i == dom:
+            if gemm_events is not None and i in gemm_events:
                 # events around the GEMM launch(es) alone, on their stream
                 tr = trs[counter[0] % copies]
                 E.input_transform(xs[i], suh, xh[i])
-                gemm_events[0].record(stream)
+                gemm_events[i][0].record(stream)
                 if split:
                     E.gemm_splitk(xh[i], tr, bits, cb, svh, layer.shard_cols, accs[i], out=ys[i])
                 else:
                     E.gemm(xh[i], tr, bits, cb, svh, layer.shard_cols, out=ys[i])
-                gemm_events[1].record(stream)
+                gemm_events[i][1].record(stream)
             else:
                 one_linear(i, counter[0])
             counter[0] += 1
@@ -256,13 +277,15 @@ def run_gpu(args, wl_name):
     time.sleep(0.3)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    dom_ev = [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(args.steps)]
+    call_ev = [{i: [torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                for i in {dom, small}} for _ in range(args.steps)]
     t0.record(stream)
     for j in range(args.steps):
-        step(gemm_events=dom_ev[j])
+        step(gemm_events=call_ev[j])
     t1.record(stream)
     torch.cuda.synchronize()
-    dom_launch_s = sum(a.elapsed_time(b) for a, b in dom_ev) / args.steps / 1e3
+    dom_launch_s = sum(ev[dom][0].elapsed_time(ev[dom][1]) for ev in call_ev) / args.steps / 1e3
+    small_launch_s = sum(ev[small][0].elapsed_time(ev[small][1]) for ev in call_ev) / args.steps / 1e3
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -365,6 +388,15 @@ def run_gpu(args, wl_name):
                 "timed": f"CUDA events around the call in each of the {args.steps} timed steps",
                 "traffic": recorded_traffic(f"{wl_name}:m={md}")}
 
+    # The HBM-bound regime's kernel: the m = 16 call, against the copy bandwidth.
+    ms_small = ms[small]
+    achieved_s = k * n * bits / 8 / small_launch_s / 1e9
+    roofline_small = {"bound": "hbm", "achieved": round(achieved_s, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                      "frac": round(achieved_s / peaks["hbm_gbs"], 4), "peak_source": peak_src + " copy bandwidth",
+                      "kernel": f"exl3 GEMM at m={ms_small}", "launch_us": round(small_launch_s * 1e6, 2),
+                      "timed": f"CUDA events around the call in each of the {args.steps} timed steps",
+                      "traffic": recorded_traffic(f"{wl_name}:m={ms_small}")}
+
     sweep = []
     for i, m in enumerate(ms):
         t = per_m_s[i]
@@ -451,14 +483,12 @@ def run_gpu(args, wl_name):
             "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "fp16 products, fp32 accumulation, bf16 out",
             "data": "synthetic (seeded; random trellis words, sign*U(0.8,1.2) scales, N(0,1) bf16 activations)",
-            "config": {"workload": desc, "k": k, "n": n, "bits": bits, "codebook": ["3inst", "mcg", "mul1"][cb],
-                       "m": ms, "split_k": split, "parallelism": f"replicas x{world} (rows independent)",
-                       "tile_shape": "autotuned in warm-up" if args.autotune else "cost model",
-                       "l2": f"weights rotate over {copies} copies ({copies * wbytes / 1e6:.0f} MB > 3x L2)"},
+            "config": workload_config(args, wl_name, world),
             "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline,
+            "roofline_small": roofline_small,
             "sweep": sweep,
             "clocks": clk,
             "ruler": {"copy_gbps": round(ruler_gbps, 1), "of_hbm_peak": round(ruler_gbps / peaks["hbm_gbs"], 3)},
@@ -592,7 +622,7 @@ def run_reference(args, wl_name):
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(el / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "k": k, "n": n, "bits": bits, "m": ms},
+        "config": workload_config(args, wl_name, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": cpu,
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

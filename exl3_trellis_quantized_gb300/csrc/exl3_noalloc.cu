@@ -8,8 +8,6 @@
 // a fixed array compiled into this library.  The array occupies
 // EXL3_NOALLOC_SCRATCH_BYTES on every GPU that loads the library, for as long as
 // the process runs.
-#include <mutex>
-
 #include "../../include/exl3.h"
 
 namespace {
@@ -20,22 +18,13 @@ constexpr size_t kScratchFloats = EXL3_NOALLOC_SCRATCH_BYTES / sizeof(float);
 // not a device address: the address is obtained with cudaGetSymbolAddress below.
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device, resolved once per
-// device (with that device current) and cached.
+// Device address of the scratch array in the current device's context.  It is
+// looked up on every call (a table lookup that allocates nothing), so a context
+// torn down and rebuilt by cudaDeviceReset never leaves a stale address behind.
 exl3_status_t scratch_for_current_device(float** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return EXL3_ECUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return EXL3_ECUDA;
-    g_scratch_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return EXL3_ECUDA;
+  *out = static_cast<float*>(p);
   return EXL3_OK;
 }
 

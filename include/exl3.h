@@ -25,6 +25,19 @@
  *  - k and n are multiples of 128 (whole Hadamard blocks; cuda-exl3 README,
  *    "Loading into a dim vLLM has padded").  bits is 1..8 (cuda-exl3 README,
  *    "What is supported").
+ *  - Padded dims (same passage).  A dim padded for tensor parallelism is padded
+ *    by whole 128-blocks, and the library needs nothing special for it:
+ *      output (n) pad: the caller sets svh = 0 on the pad columns; those outputs
+ *        are then exactly zero whatever trellis words sit behind them (every
+ *        code decodes finite), and the real columns are unchanged because the
+ *        output rotation mixes only inside a 128-column block;
+ *      input (k) pad: when loading a checkpoint layer of K_real rows into a dim
+ *        of K rows, the caller copies the K_real/16 trellis tile rows and the
+ *        K_real suh entries per shard that exist and zeroes the rest (it must
+ *        not read past the checkpoint's end), and the activations carry exact
+ *        zeros on the pad positions (the producing layer's padded output
+ *        already does).  The result equals the unpadded layer's, byte for byte
+ *        for exl3_gemm (the extra k16 steps add exact zeros).
  */
 #ifndef EXL3_H
 #define EXL3_H
@@ -137,11 +150,17 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
  * (never on m), so rows stay byte-equal across batch sizes.  It is a pure host
  * function.  exl3_splitk_workspace_bytes(m, k, n) = P * m * n * 4.
  *
- *   acc        device, fp32 [P][m][n].  Must be all zero on entry; it is all zero
- *              again when the call's work completes.  Calls that share one acc
- *              must be ordered on one stream.
+ *   acc        device, fp32 [P][m][n].  Its contents on entry do not matter:
+ *              each part stores every partial it owns (plain stores, no
+ *              accumulation into acc) before the epilogue reads it.  The
+ *              epilogue writes zeros back, the pages' re-zeroed accumulator,
+ *              so acc is all zero when the call's work completes; nothing
+ *              relies on that.  Calls that share one acc must be ordered on
+ *              one stream.
  *   acc_bytes  size of acc in bytes; smaller than the workspace size -> EXL3_EWORKSPACE
  *   other arguments as exl3_gemm.
+ * If a kernel of the call gives up on a bounded wait (exl3_device_status then
+ * reports it), its part skips its stores and y is undefined for that call.
  */
 int32_t exl3_splitk_parts(int64_t k, int64_t n);
 size_t exl3_splitk_workspace_bytes(int64_t m, int64_t k, int64_t n);
@@ -243,13 +262,17 @@ exl3_status_t exl3_moe_combine(const void* y, exl3_dtype_t y_dtype, int64_t rows
  *  - Size limit: exl3_splitk_workspace_bytes(m, k, n) must not exceed
  *    EXL3_NOALLOC_SCRATCH_BYTES; a larger request returns EXL3_EWORKSPACE and
  *    launches nothing (use exl3_gemm_splitk with your own workspace instead).
- *  - The first call on a device looks up the scratch array's device address
- *    (with that device current) and caches it; make that first call before any
- *    stream capture on that device.
+ *  - Each call looks up the scratch array's address in the current device's
+ *    context (a lookup that allocates nothing), so no address outlives a
+ *    context: after cudaDeviceReset the next call uses the new context's array.
+ *    Loading the module on a device happens at its first call; make that call
+ *    before any stream capture on that device.
  *  - Every call shares the one array.  Calls whose work may overlap on the GPU
  *    (different streams, or different threads without ordering) race on it and
  *    give wrong results; order them on one stream.  Each call overwrites every
  *    partial it reads, so what an earlier call left behind does no harm.
+ *  - As for exl3_gemm_splitk, y is undefined for a call during which
+ *    exl3_device_status records a wait that gave up.
  */
 #define EXL3_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 exl3_status_t exl3_gemm_splitk_noalloc(const uint16_t* xh, int64_t m, int64_t k, const int16_t* trellis,

@@ -3,14 +3,17 @@ timed once per distinct layer shape and batch bucket, cached, and never tuned
 while a CUDA graph is being captured.
 
 Every tile shape computes the same bytes, so the tuned launch must equal the
-cost model's launch byte for byte; the cache must hold one key per distinct
-call shape; a captured launch must neither tune nor add a key.
+cost model's launch byte for byte and meet the oracle's per-column bar; the
+cache must hold one key per distinct call shape; a captured launch must neither
+tune nor add a key.
 """
 import pytest
 import torch
 
 import exl3_trellis_quantized_gb300 as E
 from exl3_trellis_quantized_gb300 import synthetic
+from oracle import exl3_oracle as O
+from oracle_check import assert_columns
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -25,15 +28,22 @@ def _tuner_off():
     assert E.device_status() == 0
 
 
-def _layer(k, cols, bits, cb, seed):
+def _layer(k, cols, bits, cb, seed, host=False):
     layer = synthetic.make_layer(k, cols, bits, cb, seed=seed)
-    return layer.trellis.to(DEV), layer.suh.to(DEV), layer.svh.to(DEV), layer.shard_cols
+    dev = (layer.trellis.to(DEV), layer.suh.to(DEV), layer.svh.to(DEV), layer.shard_cols)
+    return dev + (layer,) if host else dev
+
+
+def _against_oracle(y, x, layer):
+    ref = O.linear(x.float().cpu().numpy(), layer.trellis.numpy(), layer.bits, layer.codebook,
+                   layer.suh.float().numpy(), layer.svh.float().numpy(), layer.shard_cols)
+    assert_columns(y.float().cpu().numpy(), ref, "tuned launch")
 
 
 @pytest.mark.parametrize("m", [1, 16, 100, 300])
 @pytest.mark.parametrize("bits,cb", [(2, 0), (4, 1), (6, 2)])
 def test_tuned_equals_model(m, bits, cb):
-    tr, suh, svh, cols = _layer(1024, [512, 256], bits, cb, seed=7000 + bits)
+    tr, suh, svh, cols, layer = _layer(1024, [512, 256], bits, cb, seed=7000 + bits, host=True)
     x = synthetic.make_x(m, 1024, seed=7001).to(DEV)
     xh = E.input_transform(x, suh)
     y_model = E.gemm(xh, tr, bits, cb, svh, cols)
@@ -44,14 +54,16 @@ def test_tuned_equals_model(m, bits, cb):
     assert E.autotune_entries() == 1
     assert torch.equal(y_tuned.view(torch.int16), y_model.view(torch.int16))
     assert torch.equal(y_again.view(torch.int16), y_model.view(torch.int16))
+    _against_oracle(y_tuned, x, layer)
 
 
 def test_split_k_tuned_equals_model():
     k, n, bits, cb, m = 4096, 256, 3, 1, 24
-    tr, suh, svh, cols = _layer(k, [n], bits, cb, seed=7100)
+    tr, suh, svh, cols, layer = _layer(k, [n], bits, cb, seed=7100, host=True)
     parts = E.splitk_parts(k, n)
     assert parts > 1
-    xh = E.input_transform(synthetic.make_x(m, k, seed=7101).to(DEV), suh)
+    x = synthetic.make_x(m, k, seed=7101).to(DEV)
+    xh = E.input_transform(x, suh)
     acc = torch.zeros(E.splitk_workspace_bytes(m, k, n) // 4, dtype=torch.float32, device=DEV)
     y_model = E.gemm_splitk(xh, tr, bits, cb, svh, cols, acc)
     E.set_autotune(True)
@@ -60,6 +72,7 @@ def test_split_k_tuned_equals_model():
     assert E.autotune_entries() == 1
     assert torch.equal(y_tuned.view(torch.int16), y_model.view(torch.int16))
     assert not bool(acc.any()), "the epilogue leaves the workspace zeroed"
+    _against_oracle(y_tuned, x, layer)
 
 
 def test_keys_by_bucket_and_shape():

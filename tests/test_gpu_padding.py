@@ -7,6 +7,9 @@ because the Hadamard mixes only inside a 128-column block.
 
 Input side: the producing layer's pad positions are exact zeros, so suh there
 cannot reach the output, and zero input blocks add exact zeros to every sum.
+The caller builds a padded-K layer from a checkpoint by copying the k16 tile
+rows and suh entries that exist and zeroing the rest (the same page, "copy what
+exists and zero the rest").
 """
 import numpy as np
 import pytest
@@ -14,6 +17,8 @@ import torch
 
 import exl3_trellis_quantized_gb300 as E
 from exl3_trellis_quantized_gb300 import synthetic
+from oracle import exl3_oracle as O
+from oracle_check import assert_columns, oracle_linear
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -36,6 +41,10 @@ def test_output_pad_blocks_are_exact_zeros(cb, m):
     y = E.gemm(xh, tr, bits, cb, svh, [0, n_pad])
     torch.cuda.synchronize()
     assert bool((y[:, n_real:].float() == 0).all()), "pad columns must be exactly zero"
+    # the padded launch against the oracle of the padded layer (svh zero on the pad)
+    ref = oracle_linear(O, x, padded, svh=svh.cpu())
+    assert not ref[:, n_real:].any()
+    assert_columns(y.float().cpu().numpy(), ref, "padded output")
     # the real columns equal a launch over the real columns alone
     tr_real = tr[:, : n_real // 16].contiguous()
     y_real = E.gemm(xh, tr_real, bits, cb, svh[:n_real].contiguous(), [0, n_real])
@@ -74,3 +83,46 @@ def test_input_pad_blocks_add_exact_zeros(m):
     y_real = E.gemm(E.input_transform(x_real, suh[:, :k_real].contiguous()), tr_real, bits, cb, svh, [0, n])
     assert torch.equal(y_pad.view(torch.int16), y_real.view(torch.int16))
     assert np.isfinite(y_pad.float().cpu().numpy()).all()
+
+
+def pad_k_layer(trellis, suh, k_pad):
+    """The caller's padded-K load: copy the k16 tile rows and suh entries that
+    exist, zero the rest (the pad must be whole 128-row blocks)."""
+    k_real = trellis.shape[0] * 16
+    assert k_pad % 128 == 0 and k_real % 128 == 0 and k_pad >= k_real
+    tr = torch.zeros((k_pad // 16,) + tuple(trellis.shape[1:]), dtype=trellis.dtype, device=trellis.device)
+    tr[: k_real // 16] = trellis
+    su = torch.zeros((suh.shape[0], k_pad), dtype=suh.dtype, device=suh.device)
+    su[:, :k_real] = suh
+    return tr, su
+
+
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("bits,cb,m", [(4, 1, 7), (6, 0, 130), (3, 2, 33)])
+def test_padded_k_load_matches_oracle_of_unpadded_layer(bits, cb, m, split):
+    """A checkpoint layer of K = 384 loaded into a dim padded to 640 (two whole
+    pad blocks), fed activations whose pad positions are exact zeros (as the
+    producing layer's padded output is): the output is the oracle's output of
+    the unpadded layer, and the bytes of the unpadded launch."""
+    k_real, k_pad, n = 384, 640, 256
+    layer = synthetic.make_layer(k_real, [n], bits, cb, seed=5400 + bits)
+    tr_pad, suh_pad = pad_k_layer(layer.trellis.to(DEV), layer.suh.to(DEV), k_pad)
+    svh = layer.svh.to(DEV)
+    x = synthetic.make_x(m, k_real, seed=5401).to(DEV)
+    x_pad = torch.zeros((m, k_pad), dtype=x.dtype, device=DEV)
+    x_pad[:, :k_real] = x
+
+    def run(xx, tr, su):
+        acc = None
+        if split:
+            acc = torch.zeros(max(1, E.splitk_workspace_bytes(m, xx.shape[1], n) // 4), dtype=torch.float32,
+                              device=DEV)
+        return E.linear(xx, tr, bits, cb, su, svh, layer.shard_cols, acc=acc)
+
+    y_pad = run(x_pad, tr_pad, suh_pad)
+    y_real = run(x, layer.trellis.to(DEV), layer.suh.to(DEV))
+    torch.cuda.synchronize()
+    assert_columns(y_pad.float().cpu().numpy(), oracle_linear(O, x, layer), "padded-K load")
+    if not split:  # the same k16 chain plus exact zeros
+        assert torch.equal(y_pad.view(torch.int16), y_real.view(torch.int16))
+    assert E.device_status() == 0

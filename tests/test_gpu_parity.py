@@ -17,10 +17,10 @@ import exl3_trellis_quantized_gb300 as E
 from exl3_trellis_quantized_gb300 import binding as B
 from exl3_trellis_quantized_gb300 import synthetic
 from oracle import exl3_oracle as O
+from oracle_check import TOL, assert_columns
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
-TOL = 4e-3
 
 
 @pytest.fixture(autouse=True)
@@ -47,12 +47,7 @@ def _oracle(x, layer, col_blocks=None):
                     layer.shard_cols, col_blocks=col_blocks)
 
 
-def _assert_columns(got, ref, what=""):
-    colmax = np.abs(ref).max(axis=0)
-    err = np.abs(got - ref)
-    bad = err > TOL * colmax
-    assert not bad.any(), f"{what}: {bad.sum()} values out of tolerance, worst err/colmax {np.max(err / colmax):.3e}"
-    return float(np.max(err / colmax))
+_assert_columns = assert_columns
 
 
 def _run(layer, x, out_dtype, split, m=None):
@@ -287,33 +282,75 @@ def test_empty_batch():
 # ---------------------------------------------------------------------------
 
 FULL = [
-    # name, k, shard widths, bits, codebook, m, split
-    ("single_2048x4096_4b_mcg", 2048, [4096], 4, 1, 16, False),
-    ("q_proj_5120x12288_6b_mcg", 5120, [12288], 6, 1, 4096, False),
-    ("gate_up_5120x2x17408_5b_mul1", 5120, [17408, 17408], 5, 2, 512, False),
-    ("down_17408x5120_6b_mul1_splitk", 17408, [5120], 6, 2, 512, True),
-    ("lm_head_4096x154880_6b_3inst", 4096, [154880], 6, 0, 16, False),
-    ("proj_12288x4096_5b_mcg", 12288, [4096], 5, 1, 2048, False),
+    # name, k, shard widths, bits, codebook, m, split: every layer at the batch
+    # sizes the benchmark times it at (m = 1 is covered by the byte-equality
+    # test below, whose rows equal those of the checked batches)
+    ("single_2048x4096_4b_mcg_m16", 2048, [4096], 4, 1, 16, False),
+    ("q_proj_5120x12288_6b_mcg_m16", 5120, [12288], 6, 1, 16, False),
+    ("q_proj_5120x12288_6b_mcg_m512", 5120, [12288], 6, 1, 512, False),
+    ("q_proj_5120x12288_6b_mcg_m4096", 5120, [12288], 6, 1, 4096, False),
+    ("gate_up_5120x2x17408_5b_mul1_m16", 5120, [17408, 17408], 5, 2, 16, False),
+    ("gate_up_5120x2x17408_5b_mul1_m512", 5120, [17408, 17408], 5, 2, 512, False),
+    ("down_17408x5120_6b_mul1_splitk_m16", 17408, [5120], 6, 2, 16, True),
+    ("down_17408x5120_6b_mul1_splitk_m512", 17408, [5120], 6, 2, 512, True),
+    ("lm_head_4096x154880_6b_3inst_m16", 4096, [154880], 6, 0, 16, False),
+    ("lm_head_4096x154880_6b_3inst_m512", 4096, [154880], 6, 0, 512, False),
+    ("lm_head_4096x154880_6b_3inst_m2048", 4096, [154880], 6, 0, 2048, False),
+    ("proj_12288x4096_5b_mcg_m16", 12288, [4096], 5, 1, 16, False),
+    ("proj_12288x4096_5b_mcg_m512", 12288, [4096], 5, 1, 512, False),
+    ("proj_12288x4096_5b_mcg_m2048", 12288, [4096], 5, 1, 2048, False),
 ]
+
+
+def _sampled_blocks(layer):
+    nb = layer.n // 128
+    blocks = {0, nb // 2, nb - 1}
+    for s in range(1, len(layer.shard_cols) - 1):  # first block of every further shard
+        blocks.add(layer.shard_cols[s] // 128)
+    return sorted(blocks)
 
 
 @pytest.mark.parametrize("name,k,widths,bits,cb,m,split", FULL, ids=[f[0] for f in FULL])
 def test_full_size_sampled(name, k, widths, bits, cb, m, split):
-    layer = synthetic.make_layer(k, widths, bits, cb, seed=2000 + len(name))
+    """Every row of sampled 128-column blocks against the oracle, at full size."""
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=2000 + k + len(widths))
     x = synthetic.make_x(m, k, seed=2000)
     y, acc = _run(layer, x, torch.bfloat16, split)
-    rows = list(range(m))  # the column max of the tolerance is over every row of the batch
+    blocks = _sampled_blocks(layer)
     nb = layer.n // 128
-    blocks = sorted({0, nb // 2, nb - 1})
-    for s in range(1, len(widths)):  # first block of every further shard
-        blocks.append(layer.shard_cols[s] // 128)
-    blocks = sorted(set(blocks))
-    ref = _oracle(x[rows], layer, blocks)
-    got = _np(y)[rows].reshape(len(rows), nb, 128)[:, blocks].reshape(len(rows), -1)
+    ref = _oracle(x, layer, blocks)  # the column max of the tolerance is over every row of the batch
+    got = _np(y.view(m, nb, 128)[:, blocks].reshape(m, -1))
     _assert_columns(got, ref, name)
     assert not torch.isnan(y.float()).any()
     if split:
         assert not acc.any()
+
+
+BENCH_SETS = [
+    # name, k, shard widths, bits, codebook, split, the benchmark's batch sizes
+    ("q_proj", 5120, [12288], 6, 1, False, [1, 16, 32, 64, 128, 256, 512, 1024, 2048, 4096]),
+    ("gate_up", 5120, [17408, 17408], 5, 2, False, [1, 16, 128, 512]),
+    ("down_splitk", 17408, [5120], 6, 2, True, [1, 16, 128, 512]),
+    ("lm_head", 4096, [154880], 6, 0, False, [1, 16, 512, 2048]),
+    ("proj_12288x4096", 12288, [4096], 5, 1, False, [1, 16, 512, 2048]),
+    ("single_2048x4096", 2048, [4096], 4, 1, False, [1, 16]),
+]
+
+
+@pytest.mark.parametrize("name,k,widths,bits,cb,split,ms", BENCH_SETS, ids=[b[0] for b in BENCH_SETS])
+def test_full_size_rows_byte_equal_across_bench_batches(name, k, widths, bits, cb, split, ms):
+    """Each row's output bytes do not depend on the batch it is computed in:
+    the first m rows of the largest benchmarked batch equal a launch of those m
+    rows alone, for every batch size the benchmark times the layer at (each one
+    takes its own tile plan)."""
+    layer = synthetic.make_layer(k, widths, bits, cb, seed=2100 + k)
+    x = synthetic.make_x(max(ms), k, seed=2101)
+    big, _ = _run(layer, x, torch.bfloat16, split)
+    for m in ms[:-1]:
+        y, acc = _run(layer, x, torch.bfloat16, split, m=m)
+        assert torch.equal(y.view(torch.int16), big[:m].view(torch.int16)), f"{name}: rows differ at m={m}"
+        if split:
+            assert not acc.any()
 
 
 SPLIT_CASES = [
