@@ -89,11 +89,13 @@ struct TmCfg {
 
 // State of relative value D of a thread's window from its aligned views
 // (r[i] = window bits [32 i, 32 i + 32), h[i] = bits [32 i + 16, 32 i + 48)).
-// One operation when the state sits at bit 0, 8 or 16 of a view; otherwise the
-// bits above it are dropped by a multiply with 2^(16 - q) on the integer
-// multiply pipe (the hashes of 3inst and mcg leave that pipe room) or, for
-// mul1, whose byte sums already load it, by a shift on the ALU pipe, and the
-// bits below by a right shift of 16.
+// One operation when the state sits at bit 0, 8 or 16 of a view; a state that
+// straddles two aligned views elsewhere is one funnel shift of the pair plus a
+// mask (so no half view is built for it); otherwise the bits above it are
+// dropped by a multiply with 2^(16 - q) on the integer multiply pipe (the
+// hashes of 3inst and mcg leave that pipe room) or, for mul1, whose byte sums
+// already load it, by a shift on the ALU pipe, and the bits below by a right
+// shift of 16.
 template <int BITS, int D, int CB, int V>
 __device__ __forceinline__ uint32_t col_state(const uint32_t (&r)[V], const uint32_t (&h)[V], const DecodeConsts& mc) {
   constexpr int p = D * BITS;
@@ -101,6 +103,7 @@ __device__ __forceinline__ uint32_t col_state(const uint32_t (&r)[V], const uint
   constexpr bool half = q0 > 16;               // inside the half-offset view h[v]
   constexpr int q = half ? q0 - 16 : q0;       // offset inside the chosen view
   static_assert(v < V && (!half || v + 1 < V), "state outside the views");
+  if constexpr (half && q != 0 && q != 8) return __funnelshift_r(r[v], r[v + 1], q0) & 0xFFFFu;
   const uint32_t x = half ? h[v] : r[v];
   if constexpr (q == 0) {
     return x & 0xFFFFu;
@@ -147,16 +150,23 @@ struct TmItem {
   int part;
 };
 template <int KA>
-__device__ __forceinline__ TmItem tm_item(const GemmArgs& a, int64_t w) {
-  const int64_t nblk = (a.n - a.col_base) >> 7;
-  const int64_t part = w / nblk;
+__device__ __forceinline__ TmItem tm_item(const GemmArgs& a, int64_t w64) {
+  // 32-bit index arithmetic (every warp calls this once per item): k and n are
+  // at most 2^31, so k/128 and n/128 are at most 2^24, and there are at most
+  // 16 parts, so every product below stays under 2^28
+  const uint32_t nblk = (uint32_t)((a.n - a.col_base) >> 7);
+  const uint32_t kblk = (uint32_t)(a.k >> 7);
+  const uint32_t parts = (uint32_t)a.parts;
+  const uint32_t w = (uint32_t)w64;
+  const uint32_t part = w / nblk;
   TmItem t;
-  t.c0 = a.col_base + (w - part * nblk) * 128;
+  t.c0 = a.col_base + (int64_t)(w - part * nblk) * 128;
   t.part = (int)part;
   // whole 128-row blocks of k per part
-  t.kb0 = part * (a.k >> 7) / a.parts * 2;
-  const int64_t kb1 = (part + 1) * (a.k >> 7) / a.parts * 2;
-  t.nk = (int)((kb1 - t.kb0) / KA);  // the host keeps KA a divisor of every part
+  const uint32_t kb0 = part * kblk / parts * 2;
+  const uint32_t kb1 = (part + 1) * kblk / parts * 2;
+  t.kb0 = (int64_t)kb0;
+  t.nk = (int)((kb1 - kb0) / KA);  // the host keeps KA a divisor of every part
   return t;
 }
 
