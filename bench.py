@@ -32,6 +32,12 @@ METRIC = "EXL3 linear GB/s, TFLOPS and %roofline vs batch rows m=1-4096 (1 GB300
 UNIT = "% of 1-GPU roofline (sweep SoL time / measured time, summed over GPUs)"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# The small-batch call's issue-rate roofline: SMs, maximum SM clock, and the
+# warp instructions the column decode spends per 512 decoded values (16 values
+# on each of a warp's 32 lanes), counted by ncu on the decode loop alone.
+SMS_GB300 = 152
+SM_MAX_GHZ = 2.07
+DECODE_WARP_INSTR_PER_512 = 104
 
 WORKLOADS = {
     # name: (description, k, shard widths, bits, codebook, m list, split)
@@ -397,6 +403,19 @@ def run_gpu(args, wl_name):
                       "timed": f"CUDA events around the call in each of the {args.steps} timed steps",
                       "traffic": recorded_traffic(f"{wl_name}:m={ms_small}")}
 
+    # The same call against the bound of a decode-bound launch: instruction
+    # issue.  Peak = 4 warp instructions per cycle per SM x SMs x the maximum
+    # SM clock, over the column decode's 104 warp instructions per 512 values
+    # (16 values on each of 32 lanes; ncu count of the decode loop alone).
+    issue_peak = 4.0 * SMS_GB300 * SM_MAX_GHZ * 1e9
+    values_peak = issue_peak * 512.0 / DECODE_WARP_INSTR_PER_512
+    values_s = k * n / small_launch_s
+    roofline_small_alu = {"bound": "alu", "achieved": round(values_s / 1e9, 1), "peak": round(values_peak / 1e9, 1),
+                          "unit": "G decoded values/s", "frac": round(values_s / values_peak, 4),
+                          "peak_source": f"issue rate: 4 warp instructions/cycle x {SMS_GB300} SMs x {SM_MAX_GHZ} GHz, "
+                                         f"{DECODE_WARP_INSTR_PER_512} warp instructions per 512 decoded values",
+                          "kernel": f"exl3 GEMM at m={ms_small}", "launch_us": round(small_launch_s * 1e6, 2)}
+
     sweep = []
     for i, m in enumerate(ms):
         t = per_m_s[i]
@@ -489,6 +508,7 @@ def run_gpu(args, wl_name):
             "gpu_launches": launches_per_step * args.steps,
             "roofline": roofline,
             "roofline_small": roofline_small,
+            "roofline_small_alu": roofline_small_alu,
             "sweep": sweep,
             "clocks": clk,
             "ruler": {"copy_gbps": round(ruler_gbps, 1), "of_hbm_peak": round(ruler_gbps / peaks["hbm_gbs"], 3)},
