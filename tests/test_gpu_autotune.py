@@ -34,10 +34,13 @@ def _layer(k, cols, bits, cb, seed, host=False):
     return dev + (layer,) if host else dev
 
 
-def _against_oracle(y, x, layer):
-    ref = O.linear(x.float().cpu().numpy(), layer.trellis.numpy(), layer.bits, layer.codebook,
+def _against_oracle(y, layer, m, m_case, seed):
+    """The first m rows of the case's largest batch (m_case rows; make_x gives
+    prefixes), against the oracle with the column max over that batch."""
+    x = synthetic.make_x(m_case, layer.k, seed=seed)
+    ref = O.linear(x.float().numpy(), layer.trellis.numpy(), layer.bits, layer.codebook,
                    layer.suh.float().numpy(), layer.svh.float().numpy(), layer.shard_cols)
-    assert_columns(y.float().cpu().numpy(), ref, "tuned launch")
+    assert_columns(y.float().cpu().numpy(), ref[:m], "tuned launch", ref_batch=ref)
 
 
 @pytest.mark.parametrize("m", [1, 16, 100, 300])
@@ -54,7 +57,7 @@ def test_tuned_equals_model(m, bits, cb):
     assert E.autotune_entries() == 1
     assert torch.equal(y_tuned.view(torch.int16), y_model.view(torch.int16))
     assert torch.equal(y_again.view(torch.int16), y_model.view(torch.int16))
-    _against_oracle(y_tuned, x, layer)
+    _against_oracle(y_tuned, layer, m, 300, 7001)
 
 
 def test_split_k_tuned_equals_model():
@@ -72,7 +75,7 @@ def test_split_k_tuned_equals_model():
     assert E.autotune_entries() == 1
     assert torch.equal(y_tuned.view(torch.int16), y_model.view(torch.int16))
     assert not bool(acc.any()), "the epilogue leaves the workspace zeroed"
-    _against_oracle(y_tuned, x, layer)
+    _against_oracle(y_tuned, layer, m, m, 7101)
 
 
 def test_keys_by_bucket_and_shape():
