@@ -227,6 +227,64 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
 
 
+TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16}  # tensor-memory shapes and the rows they hold
+
+
+@pytest.mark.parametrize("bits", range(1, 9))
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_tensor_memory_shapes_every_width(bits, cb):
+    """The tensor-memory kernel's column decode (16 values of one column a
+    lane) at every width and codebook: each of its shapes gives the bytes of
+    64-column strips (shape 1, whose decode takes 8 consecutive values a lane
+    into shared memory), plain and split-k, and meets the oracle."""
+    k, n = 512, 256
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=4500 + 3 * bits + cb)
+    tr, suh, svh = _dev(layer)
+    x = synthetic.make_x(32, k, seed=4501)
+    ref = _oracle(x, layer)
+    for m in (1, 7, 16, 32):
+        xh = E.input_transform(x[:m].to(DEV), suh)
+        want = B.test_gemm_shape(1, xh, tr, bits, cb, svh, layer.shard_cols)
+        assert torch.equal(E.gemm(xh, tr, bits, cb, svh, layer.shard_cols).view(torch.int16), want.view(torch.int16))
+        acc = torch.zeros(max(1, E.splitk_workspace_bytes(m, k, n) // 4), dtype=torch.float32, device=DEV)
+        want_split = B.test_gemm_shape(1, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+        assert want_split is not None
+        for shape, rows in TM_SHAPES.items():
+            if m > rows:
+                continue
+            got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols)
+            assert got is not None, f"shape {shape} refused m={m}"
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"shape {shape} m={m}: bytes differ"
+            if shape in (19, 23):  # the two-atom shapes also run split-k parts
+                got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+                assert got is not None
+                assert torch.equal(got.view(torch.int16), want_split.view(torch.int16)), f"split shape {shape} m={m}"
+                assert not bool(acc.any())
+        _assert_columns(_np(want), ref[:m], f"bits={bits} cb={cb} m={m}", ref_batch=ref)
+
+
+@pytest.mark.parametrize("m", [3, 16, 29])
+def test_tensor_memory_kernel_many_items(m):
+    """A persistent launch with several waves of work items and a ragged last
+    wave (400 column blocks over the SMs), at ragged batch sizes: bytes of the
+    column strips' launch, and the oracle on blocks of the first, a middle and
+    the last wave."""
+    k, n, bits, cb = 256, 400 * 128, 5, 1
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=4600)
+    tr, suh, svh = _dev(layer)
+    x = synthetic.make_x(32, k, seed=4601)
+    xh = E.input_transform(x[:m].to(DEV), suh)
+    rows = 16 if m <= 16 else 32
+    got = B.test_gemm_shape(23 if rows == 16 else 19, xh, tr, bits, cb, svh, layer.shard_cols)
+    strips = B.test_gemm_shape(3, xh, tr, bits, cb, svh, layer.shard_cols)  # 128 x 128 tiles, one per block
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), strips.view(torch.int16))
+    blocks = [0, 151, 152, 303, 304, 399]
+    ref = _oracle(x, layer, blocks)
+    out = _np(got).reshape(m, n // 128, 128)[:, blocks].reshape(m, -1)
+    _assert_columns(out, ref[:m], f"m={m}", ref_batch=ref)
+
+
 def test_tile_shape_rejections():
     layer = synthetic.make_layer(1024, [384], 3, 1, seed=4300)
     tr, suh, svh = _dev(layer)
