@@ -86,10 +86,12 @@ struct TcCfg {
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kAvail = kTcSmemBudget - 1024 - kCtrlBytes;
   // Ring depths: three decoded-operand slots when two activation slots and
-  // four trellis slots still fit, else two; then four activation slots for
-  // small batches (they are small), otherwise three, if four trellis slots
-  // still fit, else two; the trellis ring takes the rest.
-  static constexpr int kNW = (kAvail - 2 * kXSlot - 3 * kWSlot >= 4 * kTSlot) ? 3 : 2;
+  // four trellis slots still fit (three for small batches, whose stages are
+  // long enough that two copies in flight cover the memory latency), else
+  // two; then four activation slots for small batches (they are small),
+  // otherwise three, if four trellis slots still fit, else two; the trellis
+  // ring takes the rest.
+  static constexpr int kNW = (kAvail - 2 * kXSlot - 3 * kWSlot >= (XR < 128 ? 3 : 4) * kTSlot) ? 3 : 2;
   static constexpr int kNX = (kAvail - (XR < 128 ? 4 : 3) * kXSlot - kNW * kWSlot >= 4 * kTSlot) ? (XR < 128 ? 4 : 3) : 2;
   static constexpr int kNT0 = (kAvail - kNX * kXSlot - kNW * kWSlot) / kTSlot;
   static constexpr int kNT = kNT0 > 16 ? 16 : kNT0;
