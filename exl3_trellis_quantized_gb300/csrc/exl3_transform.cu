@@ -7,11 +7,13 @@
 // "One op per layer": every shard in one launch, x read once, the bf16 -> fp16
 // conversion folded into the same pass).
 //
-// Four lanes own one (row, 128-block): lane q of the four holds elements
-// 32q..32q+31, so a warp covers eight blocks (2 KB of x) per pass with 16-byte
-// loads and stores.  Butterfly stages of stride 1..16 stay in registers; for
-// the stride-32 and stride-64 stages the warp regroups its blocks once through
-// shared memory so that each lane holds four elements 32 apart (rotate_store).
+// The plain transform gives eight lanes to one (row, 128-block): lane p of the
+// eight holds elements 16p..16p+15, so a warp covers four blocks (1 KB of x)
+// per pass with 16-byte loads.  Butterfly stages of stride 1..8 stay in
+// registers; for the stride-16, -32 and -64 stages the warp regroups its blocks
+// once through shared memory (rotate_store16).  The SwiGLU and grouped-expert
+// transforms give four lanes to a block (32 elements each, strides 1..16 in
+// registers, 32 and 64 after the regroup: rotate_store).
 // Each stage computes (a, b) -> (a + b, a - b) on the same pairs as the plain
 // definition, so the order of fp32 adds is the fixed one.  x is read once and reused for
 // every shard.  The kernel is HBM/L2-bound: 2 bytes in, 2*S bytes out per
@@ -102,6 +104,70 @@ __device__ __forceinline__ void rotate_store(float (&v)[32], int q, float* xp, u
   }
 }
 
+// The same butterfly over eight lanes per block, 16 values a lane (elements
+// 16p..16p+15 of lane p of the eight), for the plain transform: 74 registers
+// against 110-127 for the four-lane form, so three blocks of eight warps stay
+// resident per SM instead of two (measured 3-17% faster, most at m <= 512).  Strides 1..8 run in registers; one pass through the
+// warp's shared-memory area (four blocks of 128 floats, 144 apart so the two
+// blocks of a half-warp land on different banks) regroups each lane to
+// elements 16t + 2p + e (t = 0..7, e = 0, 1), whose stride-16, -32 and -64
+// partners it then holds; the 16-byte chunks are written with their slot XORed
+// by p / 2, so a quarter-warp's writes cover all 32 banks.  Every stage maps
+// the same pairs (a, b) -> (a + b, a - b) in the same stride order, so the fp32
+// sums are the definition's.  Each lane stores 4 bytes per t, a block 32
+// contiguous bytes per t.
+__device__ __forceinline__ void rotate_store16(float (&v)[16], int p, float* xp, uint16_t* dst) {
+#pragma unroll
+  for (int st = 1; st < 16; st <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if ((i & st) == 0) {
+        const float a = v[i], b = v[i + st];
+        v[i] = a + b;
+        v[i + st] = a - b;
+      }
+    }
+  }
+  float* blk = xp + ((threadIdx.x & 31) >> 3) * 144;
+  __syncwarp();  // the previous pass's reads of xp are done
+#pragma unroll
+  for (int i4 = 0; i4 < 4; ++i4) {
+    const int slot = i4 ^ (p >> 1);
+    *reinterpret_cast<float4*>(blk + 16 * p + 4 * slot) = make_float4(v[4 * i4], v[4 * i4 + 1], v[4 * i4 + 2], v[4 * i4 + 3]);
+  }
+  __syncwarp();
+  float w[8][2];  // w[t][e] = element 16t + 2p + e
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    const float2 f = *reinterpret_cast<const float2*>(blk + 16 * t + 4 * ((p >> 1) ^ (t >> 1)) + 2 * (p & 1));
+    w[t][0] = f.x;
+    w[t][1] = f.y;
+  }
+#pragma unroll
+  for (int st = 1; st < 8; st <<= 1) {  // element strides 16, 32, 64
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      if ((t & st) == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float a = w[t][e], b = w[t + st][e];
+          w[t][e] = a + b;
+          w[t + st][e] = a - b;
+        }
+      }
+    }
+  }
+  if (dst != nullptr) {
+    uint16_t* base = dst - 16 * p + 2 * p;  // element 2p of the block
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      // 2^-4 is exact; both values rounded to fp16 by one conversion
+      const __half2 hv = __floats2half2_rn(w[t][0] * 0.0625f, w[t][1] * 0.0625f);
+      *reinterpret_cast<uint32_t*>(base + 16 * t) = *reinterpret_cast<const uint32_t*>(&hv);
+    }
+  }
+}
+
 }  // namespace
 
 template <bool X_BF16>
@@ -138,27 +204,27 @@ __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __
   // The GEMM that consumes xh may be scheduled now: it prefetches its weights
   // and waits for this grid to complete before it reads xh.
   pdl_launch_dependents();
-  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  __shared__ __align__(16) float xpose[8][4 * 144];  // per warp: its four blocks for the stride-16..64 stages
   float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int q = lane & 3;  // which 32 elements of the block
+  const int p = lane & 7;  // which 16 elements of the block
   const int64_t kb = k >> 7;
   const int64_t units = m * kb;
-  const int64_t groups = (units + 7) / 8;  // eight blocks per warp and pass
+  const int64_t groups = (units + 3) / 4;  // four blocks per warp and pass
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // The lane's unit u = g * 8 + lane / 4 advances by 8 * warps_total units a
+  // The lane's unit u = g * 4 + lane / 8 advances by 4 * warps_total units a
   // pass; its (row, block) is stepped, not divided out, each pass.
   int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int64_t step = 8 * warps_total;
+  const int64_t step = 4 * warps_total;
   const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
-  int64_t u = g * 8 + (lane >> 2);
+  int64_t u = g * 4 + (lane >> 3);
   int64_t row = u / kb, blk = u - row * kb;
   // x stays packed (bf16 / fp16 pairs) in registers; the next pass's words are
   // loaded before this pass computes, so two passes of loads are in flight
-  uint4 cur[4];
+  uint4 cur[2];
 #pragma unroll
-  for (int c = 0; c < 4; ++c)
-    cur[c] = (g < groups && u < units) ? *reinterpret_cast<const uint4*>(x + row * k + blk * 128 + 32 * q + 8 * c)
+  for (int c = 0; c < 2; ++c)
+    cur[c] = (g < groups && u < units) ? *reinterpret_cast<const uint4*>(x + row * k + blk * 128 + 16 * p + 8 * c)
                                        : make_uint4(0, 0, 0, 0);
   for (; g < groups; g += warps_total, u += step) {
     int64_t nrow = row + step_rows, nblk = blk + step_blk;
@@ -167,21 +233,21 @@ __global__ void __launch_bounds__(256) input_transform_kernel(const uint16_t* __
       nrow += 1;
     }
     const bool nok = g + warps_total < groups && u + step < units;
-    uint4 nxt[4];
+    uint4 nxt[2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
-      nxt[c] = nok ? *reinterpret_cast<const uint4*>(x + nrow * k + nblk * 128 + 32 * q + 8 * c) : make_uint4(0, 0, 0, 0);
+    for (int c = 0; c < 2; ++c)
+      nxt[c] = nok ? *reinterpret_cast<const uint4*>(x + nrow * k + nblk * 128 + 16 * p + 8 * c) : make_uint4(0, 0, 0, 0);
     const bool ok = u < units;
-    const int64_t col = ok ? blk * 128 + 32 * q : 32 * q;
+    const int64_t col = ok ? blk * 128 + 16 * p : 16 * p;
     for (int s = 0; s < num_shards; ++s) {
-      float v[32];
+      float v[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
         scale_chunk<X_BF16>(cur[c], *reinterpret_cast<const uint4*>(suh + (int64_t)s * k + col + 8 * c), v + 8 * c);
-      rotate_store(v, q, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
+      rotate_store16(v, p, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
+    for (int c = 0; c < 2; ++c) cur[c] = nxt[c];
     row = nrow;
     blk = nblk;
   }
@@ -352,7 +418,7 @@ int resident_blocks(Kernel kern, int threads) {
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
                                    int num_shards, uint16_t* xh, cudaStream_t stream) {
-  const int64_t groups = (m * (k >> 7) + 7) / 8;  // one warp pass each
+  const int64_t groups = (m * (k >> 7) + 3) / 4;  // one warp pass each (four blocks)
   const int threads = 256;
   const int64_t want = (groups + 7) / 8;
   const int cap = x_bf16 ? resident_blocks<0>(input_transform_kernel<true>, threads)

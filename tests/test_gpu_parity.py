@@ -112,6 +112,28 @@ def test_input_transform_parity(xdtype):
                              f"lo {lo[tuple(i)]!r} hi {hi[tuple(i)]!r}")
 
 
+@pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("m,k,s", [(37, 640, 3), (1, 128, 1), (300, 5120, 2)])
+def test_input_transform_bits_equal_four_lane_form(xdtype, m, k, s):
+    """The plain transform (eight lanes a block) and the grouped-expert
+    transform (four lanes a block) run the butterfly's stages in the same
+    stride order on the same pairs, so with one expert and the identity routing
+    their fp16 bytes are equal for every row and shard."""
+    g = torch.Generator().manual_seed(60 + m)
+    suh = (torch.rand(s, k, generator=g) * 0.4 + 0.8).to(torch.float16)
+    suh[:, ::3] = -suh[:, ::3]
+    x = synthetic.make_x(m, k, seed=61).to(xdtype).to(DEV)
+    plain = E.input_transform(x, suh.to(DEV))
+    block = 16
+    rows = (m + block - 1) // block * block
+    ids = torch.arange(rows, dtype=torch.int32)
+    ids[m:] = m  # padding rows (an id past the last pair)
+    grouped = E.moe_input_transform(x, ids.to(DEV), 1, torch.zeros(rows // block, dtype=torch.int32, device=DEV), block,
+                                    suh[None].to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(plain.view(torch.int16), grouped[:, :m].contiguous().view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # the layer: coverage of widths x codebooks, batch sizes, dtypes
 # ---------------------------------------------------------------------------
