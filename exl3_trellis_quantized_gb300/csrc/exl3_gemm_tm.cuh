@@ -62,11 +62,20 @@ struct TmCfg {
   static constexpr int kTrCopy = kTiles * 32 * BITS;                 // bytes of one trellis copy
   static constexpr int kTSlot = (kTrCopy + 127) / 128 * 128;
   static constexpr int kXSlot = KA * XR * 128;                       // activation rows of a stage
-  static constexpr int kNX = 4;
+  // four activation slots while they are small, three, or two when a slot
+  // is 64 KB (128 rows, four atoms)
+  static constexpr int kNX = XR <= 32 ? 4 : (kXSlot >= 64 * 1024 ? 2 : 3);
+  // tensor memory: two accumulator buffers of max(32, XR) columns (one batch
+  // row per column, one weight column per lane), then the A slots
+  static constexpr int kAccCols = XR < 32 ? 32 : XR;
+  static constexpr int kABase = 2 * kAccCols > 128 ? 2 * kAccCols : 128;
   static constexpr int kACols = 32 * KA;                             // tensor-memory columns of a stage's A
-  static constexpr int kNW = (512 - 128) / kACols > 4 ? 4 : (512 - 128) / kACols;
+  static constexpr int kNW = (512 - kABase) / kACols > 4 ? 4 : (512 - kABase) / kACols;
+  // the epilogue stages up to 32 accumulator rows at a time
+  static constexpr int kZRows = XR < 32 ? XR : 32;
+  static constexpr int kZChunks = XR / kZRows;
   static constexpr int kZStride = 128 + 4;                           // epilogue staging row stride (floats)
-  static constexpr int kZBytes = (XR * kZStride * 4 + 1023) / 1024 * 1024;
+  static constexpr int kZBytes = (kZRows * kZStride * 4 + 1023) / 1024 * 1024;
   static constexpr int kCtrlBytes = 1024;
   static constexpr int kAvail = kTmSmemBudget - 1024 - kCtrlBytes - kNX * kXSlot - kZBytes - 128;
   static constexpr int kNT0 = kAvail / kTSlot;
@@ -81,8 +90,9 @@ struct TmCfg {
   // 512 tensor-memory columns)
   static constexpr int kSmemRaw = 1024 + kCtrlBytes + kRingBytes;
   static constexpr int kSmem = kSmemRaw > 120 * 1024 ? kSmemRaw : 120 * 1024;
-  static_assert(XR % 16 == 0 && XR <= 32, "16 or 32 batch rows");
+  static_assert(XR == 16 || XR == 32 || XR == 64 || XR == 128, "16, 32, 64 or 128 batch rows");
   static_assert(kNW >= 2 && kNT >= 3, "rings too shallow");
+  static_assert(kABase + kNW * kACols <= 512, "tensor memory overflow");
   static_assert(kXSlot % 1024 == 0, "activation slots keep 1024-byte swizzle alignment");
   static_assert((2 * kNT + 2 * kNX + 2 * kNW + 4) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
@@ -314,13 +324,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           ok = false;
           break;
         }
-        const uint32_t dacc = tmem + (uint32_t)(32 * buf);
+        const uint32_t dacc = tmem + (uint32_t)(C::kAccCols * buf);
         for (int it = 0; it < t.nk; ++it) {
           ok = __all_sync(0xFFFFFFFFu, mbar_wait(&xfull[xs], xph) && mbar_wait(&afull[as], aph));
           if (!ok) break;
           tc_fence_after();
           const uint64_t dx = xdesc0 + (uint64_t)((xs * C::kXSlot) >> 4);
-          const uint32_t acol = tmem + 128u + (uint32_t)(as * C::kACols);
+          const uint32_t acol = tmem + (uint32_t)C::kABase + (uint32_t)(as * C::kACols);
 #pragma unroll
           for (int at = 0; at < KA; ++at) {
 #pragma unroll
@@ -394,7 +404,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         tc_fence_after();
         const uint32_t tb = tring_u32 + (uint32_t)(ts * C::kTSlot);
         const uint32_t b0 = tb + wo0, b1 = tb + wo1;
-        const uint32_t acol = tlane + 128u + (uint32_t)(as * C::kACols);
+        const uint32_t acol = tlane + (uint32_t)C::kABase + (uint32_t)(as * C::kACols);
         // the next row's words are loaded before this row's decode
         uint32_t wn[W::kWords];
         wn[0] = ld_shared_u32(b0);
@@ -456,41 +466,60 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       // then give up on their next wait instead of hanging
       if (!mbar_wait(&accfull[buf], (uint32_t)(i >> 1) & 1u)) break;
       tc_fence_after();
-      uint32_t q[XR];
-      tmem_ld_32x32b_cols<XR>(tmem + ((uint32_t)(32 * e) << 16) + (uint32_t)(32 * buf), q);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&accempty[buf]);
-      if (a.parts > 1) {
-        // split-k: this part's fp32 sums go straight to acc[part][row][col]
-        float* dst = a.acc + (int64_t)t.part * a.m * a.n + t.c0 + 32 * e + lane;
-#pragma unroll
-        for (int r = 0; r < XR; ++r)
-          if (r < live) dst[(a.row_base + r) * a.n] = __uint_as_float(q[r]);
-      } else {
-        // the previous item's rows have been read from the staging tile
-        if (i > 0 && !mbar_wait(zdone, (uint32_t)(i - 1) & 1u)) break;
-#pragma unroll
-        for (int r = 0; r < XR; ++r) zs[r * kZ + 32 * e + lane] = __uint_as_float(q[r]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(zfull);
-        if (!mbar_wait(zfull, (uint32_t)i & 1u)) break;
-        const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
-        const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
-        for (int rr = e; rr < live; rr += 4) {
-          const float4 z = ld_shared_v4f(smem_u32(zs) + (uint32_t)((rr * kZ + 4 * lane) * 4));
-          float v[4] = {z.x, z.y, z.z, z.w};
-          fwht128_warp(v, lane);
-          const uint32_t o0 = f32_to_out((v[0] * 0.125f) * s01.x, bf16), o1 = f32_to_out((v[1] * 0.125f) * s01.y, bf16);
-          const uint32_t o2 = f32_to_out((v[2] * 0.125f) * s23.x, bf16), o3 = f32_to_out((v[3] * 0.125f) * s23.y, bf16);
-          *reinterpret_cast<uint2*>(y + (a.row_base + rr) * a.n + t.c0 + 4 * lane) =
-              make_uint2(o0 | (o1 << 16), o2 | (o3 << 16));
+      const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
+      const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
+      bool ok = true;
+      // the accumulator in chunks of kZRows batch rows (tensor-memory columns)
+#pragma unroll 1
+      for (int c = 0; ok && c < C::kZChunks; ++c) {
+        constexpr int ZR = C::kZRows;
+        const int r0 = c * ZR;
+        uint32_t q[ZR];
+        tmem_ld_32x32b_cols<ZR>(tmem + ((uint32_t)(32 * e) << 16) + (uint32_t)(C::kAccCols * buf + r0), q);
+        tmem_ld_wait();
+        if (c + 1 == C::kZChunks) {
+          // every chunk of the buffer has been read: the MMAs may reuse it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[buf]);
         }
-        // the staging tile is rewritten by the next item
-        __syncwarp();
-        if (lane == 0) mbar_arrive(zdone);
+        if (a.parts > 1) {
+          // split-k: this part's fp32 sums go straight to acc[part][row][col]
+          float* dst = a.acc + (int64_t)t.part * a.m * a.n + t.c0 + 32 * e + lane;
+#pragma unroll
+          for (int r = 0; r < ZR; ++r)
+            if (r0 + r < live) dst[(a.row_base + r0 + r) * a.n] = __uint_as_float(q[r]);
+        } else {
+          // staging-tile use number z of this CTA: the previous use's rows have
+          // been read before the tile is rewritten
+          const uint32_t z = (uint32_t)i * (uint32_t)C::kZChunks + (uint32_t)c;
+          if (z > 0 && !mbar_wait(zdone, (z - 1u) & 1u)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int r = 0; r < ZR; ++r) zs[r * kZ + 32 * e + lane] = __uint_as_float(q[r]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(zfull);
+          if (!mbar_wait(zfull, z & 1u)) {
+            ok = false;
+            break;
+          }
+          for (int rr = e; rr < ZR && r0 + rr < live; rr += 4) {
+            const float4 zv = ld_shared_v4f(smem_u32(zs) + (uint32_t)((rr * kZ + 4 * lane) * 4));
+            float v[4] = {zv.x, zv.y, zv.z, zv.w};
+            fwht128_warp(v, lane);
+            const uint32_t o0 = f32_to_out((v[0] * 0.125f) * s01.x, bf16), o1 = f32_to_out((v[1] * 0.125f) * s01.y, bf16);
+            const uint32_t o2 = f32_to_out((v[2] * 0.125f) * s23.x, bf16), o3 = f32_to_out((v[3] * 0.125f) * s23.y, bf16);
+            *reinterpret_cast<uint2*>(y + (a.row_base + r0 + rr) * a.n + t.c0 + 4 * lane) =
+                make_uint2(o0 | (o1 << 16), o2 | (o3 << 16));
+          }
+          // the staging tile is rewritten by the next chunk or item
+          __syncwarp();
+          if (lane == 0) mbar_arrive(zdone);
+        }
       }
+      if (!ok) break;
     }
   }
   tc_fence_before();

@@ -124,7 +124,10 @@ enum class TcShape : int {
   kT128K4X16,    // BN=128, KA=4, XR=16 (m <= 16, k/128 even, no split-k)
   kS96K4X16,     // BN=96,  KA=4, XR=16 (m <= 16, k/128 even, no split-k, 384-aligned edges)
   kT128X16,      // BN=128, KA=2, XR=16 (m <= 16)
-  kLast = kT128X16,
+  kT128K4X64,    // BN=128, KA=4, XR=64 (m <= 64, k/128 even, no split-k)
+  kT128X64,      // BN=128, KA=2, XR=64 (m <= 64)
+  kT128X128,     // BN=128, KA=2, XR=128 (m <= 128)
+  kLast = kT128X128,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

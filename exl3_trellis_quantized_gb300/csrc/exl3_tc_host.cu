@@ -110,6 +110,9 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kT128K4X16: return {128, 4, 16, 1, 1};
     case TcShape::kS96K4X16: return {96, 4, 16, 1, 1};
     case TcShape::kT128X16: return {128, 2, 16, 1, 1};
+    case TcShape::kT128K4X64: return {128, 4, 64, 1, 1};
+    case TcShape::kT128X64: return {128, 2, 64, 1, 1};
+    case TcShape::kT128X128: return {128, 2, 128, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -134,6 +137,12 @@ constexpr double kRel96S = 0.85, kRel64 = 0.52, kRel64K4 = 0.68, kRel32 = 0.50, 
 // paid once per SM, not once per wave, so its rate per CTA grows with the
 // waves a layer needs (5120 x 34816: 2 waves, 4096 x 154880: 8 waves).
 double rel_tm(int64_t waves) { return waves <= 1 ? 1.02 : waves == 2 ? 1.06 : waves == 3 ? 1.15 : 1.3; }
+// The tensor-memory kernel holding 64 rows (four k atoms a stage) at
+// 32 < m <= 64 measured at the same per-SM rates as at m <= 32 (5120 x 12288:
+// 1.03 in one wave, 5120 x 34816: 1.07 in two, 4096 x 154880: 1.41 in eight);
+// holding 128 rows on two k atoms at 64 < m <= 128, about 0.89 of them (0.91,
+// 0.94, 1.22 on the same layers).
+constexpr double kRelTm128 = 0.89;
 // 256-column, 256-row tiles at 32 < m <= 128 against 128 columns, per column
 // (5120 x 34816, 4096 x 154880): fewer CTAs in whole waves.
 constexpr double kRel256Mid = 1.07;
@@ -317,6 +326,10 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r96 = edges_multiple_of(a, 384) ? small_batch_rate(a.n / 96, kRel96) : 0.0;
     const double r64 = small_batch_rate(a.n / 64, kRel64K4);
     const double r32 = small_batch_rate(a.n / 32, kRel32Full);  // 128-row strips
+    const int64_t sms = sm_count();
+    const int64_t blocks = a.n / 128;
+    const double rt = rel_tm((blocks + sms - 1) / sms) * (double)(blocks < sms ? blocks : sms);
+    if (rt >= r128 && rt >= r256 && rt >= r96 && rt >= r64 && rt >= r32) return TcShape::kT128K4X64;
     if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
     if (r128 >= r96 && r128 >= r64 && r128 >= r32) return TcShape::kN128;
     if (r32 > r96 && r32 > r64) return TcShape::kN32K4;
@@ -329,6 +342,11 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r96 = edges384 ? small_batch_rate(a.n / 96, kRel96Full) : 0.0;
     const double r64 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 64, kRel64Full) : 0.0;
     const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32Full) : 0.0;
+    const int64_t sms = sm_count();
+    const int64_t blocks = a.n / 128;
+    const double rt =
+        kRelTm128 * rel_tm((blocks + sms - 1) / sms) * (double)(blocks < sms ? blocks : sms);
+    if (rt >= r128 && rt >= r256 && rt >= r96 && rt >= r64 && rt >= r32) return TcShape::kT128X128;
     if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
     if (r32 > r128 && r32 > r96 && r32 > r64) return TcShape::kN32K4;
     if (r64 > r128 && r64 > r96) return TcShape::kN64K4;
@@ -378,11 +396,20 @@ void tc_plan(const GemmArgs& a, int64_t out[5]) {
   }
 }
 
+// The persistent tensor-memory kernel's shapes: one row group of XR rows, the
+// grid over column items only.
+static bool tm_shape(TcShape s) {
+  return s == TcShape::kT128K4 || s == TcShape::kT128 || s == TcShape::kT128K4X16 || s == TcShape::kT128X16 ||
+         s == TcShape::kT128K4X64 || s == TcShape::kT128X64 || s == TcShape::kT128X128;
+}
+
 bool tc_shape_supported(int shape, const GemmArgs& a) {
   if (shape < 0 || shape > (int)TcShape::kLast) return false;
   const TcShape s = (TcShape)shape;
   const ShapeDims d = dims_of(s);
-  if (d.xr < 128 && a.m > d.xr) return false;  // small-batch shapes hold XR rows
+  // small-batch shapes hold XR rows; the tensor-memory kernel holds XR rows
+  // whatever XR is (it has no row groups)
+  if ((d.xr < 128 || tm_shape(s)) && a.m > d.xr) return false;
   // several atoms per stage: k must hold whole stages, and no split-k
   if (d.ka > 2 && ((a.k / 128) % (d.ka / 2) != 0 || a.parts > 1)) return false;
   // n and every shard edge fall on whole CTA spans: lcm(BN, 128) columns (a

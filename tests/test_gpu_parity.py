@@ -240,16 +240,16 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
             if split:
                 assert bool((acc == 0).all()), f"shape {shape} m={m}: workspace not re-zeroed"
     # the cases reach every shape that their sizes allow
-    need = {1, 2, 3, 4, 6, 19, 23} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
+    need = {1, 2, 3, 4, 6, 19, 23, 25, 26} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     need |= {10, 11} if all(w % 384 == 0 for w in widths) else set()
     if not split and (k // 128) % 2 == 0:
-        need |= {0, 8, 13, 15, 16, 17, 18, 21} | ({9, 14, 20, 22} if all(w % 384 == 0 for w in widths) else set())
+        need |= {0, 8, 13, 15, 16, 17, 18, 21, 24} | ({9, 14, 20, 22} if all(w % 384 == 0 for w in widths) else set())
     if not split and k % 512 == 0:
         need |= {12}
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
 
 
-TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16}  # tensor-memory shapes and the rows they hold
+TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16, 24: 64, 25: 64, 26: 128}  # tensor-memory shapes and their rows
 
 
 @pytest.mark.parametrize("bits", range(1, 9))
@@ -257,19 +257,21 @@ TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16}  # tensor-memory shapes and the row
 def test_tensor_memory_shapes_every_width(bits, cb):
     """The tensor-memory kernel's column decode (16 values of one column a
     lane) at every width and codebook: each of its shapes gives the bytes of
-    64-column strips (shape 1, whose decode takes 8 consecutive values a lane
-    into shared memory), plain and split-k, and meets the oracle."""
+    the shared-memory kernel's tiles (64-column strips, shape 1, up to 32 rows;
+    128 x 128 tiles, shape 3, above; their decode takes 8 consecutive values a
+    lane), plain and split-k, and meets the oracle."""
     k, n = 512, 256
     layer = synthetic.make_layer(k, [n], bits, cb, seed=4500 + 3 * bits + cb)
     tr, suh, svh = _dev(layer)
-    x = synthetic.make_x(32, k, seed=4501)
+    x = synthetic.make_x(128, k, seed=4501)
     ref = _oracle(x, layer)
-    for m in (1, 7, 16, 32):
+    for m in (1, 7, 16, 32, 50, 64, 100, 128):
         xh = E.input_transform(x[:m].to(DEV), suh)
-        want = B.test_gemm_shape(1, xh, tr, bits, cb, svh, layer.shard_cols)
+        ref_shape = 1 if m <= 32 else 3
+        want = B.test_gemm_shape(ref_shape, xh, tr, bits, cb, svh, layer.shard_cols)
         assert torch.equal(E.gemm(xh, tr, bits, cb, svh, layer.shard_cols).view(torch.int16), want.view(torch.int16))
         acc = torch.zeros(max(1, E.splitk_workspace_bytes(m, k, n) // 4), dtype=torch.float32, device=DEV)
-        want_split = B.test_gemm_shape(1, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+        want_split = B.test_gemm_shape(ref_shape, xh, tr, bits, cb, svh, layer.shard_cols, acc)
         assert want_split is not None
         for shape, rows in TM_SHAPES.items():
             if m > rows:
@@ -277,7 +279,7 @@ def test_tensor_memory_shapes_every_width(bits, cb):
             got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols)
             assert got is not None, f"shape {shape} refused m={m}"
             assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"shape {shape} m={m}: bytes differ"
-            if shape in (19, 23):  # the two-atom shapes also run split-k parts
+            if shape in (19, 23, 25, 26):  # the two-atom shapes also run split-k parts
                 got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols, acc)
                 assert got is not None
                 assert torch.equal(got.view(torch.int16), want_split.view(torch.int16)), f"split shape {shape} m={m}"
@@ -285,7 +287,7 @@ def test_tensor_memory_shapes_every_width(bits, cb):
         _assert_columns(_np(want), ref[:m], f"bits={bits} cb={cb} m={m}", ref_batch=ref)
 
 
-@pytest.mark.parametrize("m", [3, 16, 29])
+@pytest.mark.parametrize("m", [3, 16, 29, 61, 100])
 def test_tensor_memory_kernel_many_items(m):
     """A persistent launch with several waves of work items and a ragged last
     wave (400 column blocks over the SMs), at ragged batch sizes: bytes of the
@@ -294,10 +296,10 @@ def test_tensor_memory_kernel_many_items(m):
     k, n, bits, cb = 256, 400 * 128, 5, 1
     layer = synthetic.make_layer(k, [n], bits, cb, seed=4600)
     tr, suh, svh = _dev(layer)
-    x = synthetic.make_x(32, k, seed=4601)
+    x = synthetic.make_x(128, k, seed=4601)
     xh = E.input_transform(x[:m].to(DEV), suh)
-    rows = 16 if m <= 16 else 32
-    got = B.test_gemm_shape(23 if rows == 16 else 19, xh, tr, bits, cb, svh, layer.shard_cols)
+    shape = 23 if m <= 16 else 19 if m <= 32 else 24 if m <= 64 else 26
+    got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols)
     strips = B.test_gemm_shape(3, xh, tr, bits, cb, svh, layer.shard_cols)  # 128 x 128 tiles, one per block
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int16), strips.view(torch.int16))

@@ -8,7 +8,7 @@ from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
 (N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
- N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16) = range(24)
+ N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16, T128K4X64, T128X64, T128X128) = range(27)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -36,7 +36,12 @@ def test_q_proj_plan(m, want):
     (64, 12416, 4096, None, N128), (100, 12416, 4096, None, N128),  # odd k/128: no four-atom strips
     (64, 4096, 2048, None, N32K4),  # 16 blocks: 64 strips of 32 columns
     (128, 5120, 6144, None, N64K4), (100, 5120, 12288, None, N96),
-    (48, 5120, 34816, [0, 17408, 34816], N256R2), (128, 4096, 154880, None, N256R2),  # wide: 256-column tiles
+    # wide layers: the tensor-memory kernel holding 64 rows (four atoms) or 128
+    # rows (two atoms) where its persistent waves beat 256-column tiles
+    (48, 5120, 34816, [0, 17408, 34816], T128K4X64), (64, 4096, 154880, None, T128K4X64),
+    (128, 4096, 154880, None, T128X128), (100, 4096, 154880, None, T128X128),
+    (128, 5120, 34816, [0, 17408, 34816], N256R2),  # two waves of items: 256-column tiles stay ahead
+    (48, 4224, 154880, None, T128X128),  # odd k/128: no four-atom tiles, the 128-row items
 ])
 def test_mid_batch_plan(m, k, n, cols, want):
     assert plan(m, k, n, cols)[0] == want
