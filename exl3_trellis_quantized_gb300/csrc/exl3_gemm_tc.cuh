@@ -858,6 +858,7 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kT128K4X64: return launch_tm_variant<BITS, CB, 4, 64>(maps, p, stream);
     case TcShape::kT128X64: return launch_tm_variant<BITS, CB, 2, 64>(maps, p, stream);
     case TcShape::kT128X128: return launch_tm_variant<BITS, CB, 2, 128>(maps, p, stream);
+    case TcShape::kS96K4X64: return launch_tc_variant<BITS, CB, 96, 1, 4, 64, 1, false, true>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }

@@ -127,7 +127,8 @@ enum class TcShape : int {
   kT128K4X64,    // BN=128, KA=4, XR=64 (m <= 64, k/128 even, no split-k)
   kT128X64,      // BN=128, KA=2, XR=64 (m <= 64)
   kT128X128,     // BN=128, KA=2, XR=128 (m <= 128)
-  kLast = kT128X128,
+  kS96K4X64,     // BN=96,  KA=4, XR=64 (m <= 64, k/128 even, no split-k, 384-aligned edges)
+  kLast = kS96K4X64,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.

@@ -113,6 +113,7 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kT128K4X64: return {128, 4, 64, 1, 1};
     case TcShape::kT128X64: return {128, 2, 64, 1, 1};
     case TcShape::kT128X128: return {128, 2, 128, 1, 1};
+    case TcShape::kS96K4X64: return {96, 4, 64, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
 }
@@ -333,7 +334,10 @@ TcShape choose_shape(const GemmArgs& a) {
     if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
     if (r128 >= r96 && r128 >= r64 && r128 >= r32) return TcShape::kN128;
     if (r32 > r96 && r32 > r64) return TcShape::kN32K4;
-    return r96 >= r64 ? TcShape::kN96M64K4 : TcShape::kN64M64K4;
+    // the 96-column strips with swapped operands: the 64 rows are the narrow
+    // operand, not half of a padded 128-row one (5120 x 12288, m = 33 to 64:
+    // 2-4% faster than the unswapped strips)
+    return r96 >= r64 ? TcShape::kS96K4X64 : TcShape::kN64M64K4;
   }
   if (a.m <= 128) {
     // as for small batches: 96-column tiles put a 96-block layer on 128 SMs

@@ -332,11 +332,12 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
  *         split-k, n and shard edges multiples of 384), 21 and 22 = 18 and 20
  *         holding 16 rows (m <= 16), 23 = 19 holding 16 rows (m <= 16),
  *         24 = 18 holding 64 rows (m <= 64), 25 = 19 holding 64 rows
- *         (m <= 64), 26 = 19 holding 128 rows (m <= 128).
+ *         (m <= 64), 26 = 19 holding 128 rows (m <= 128), 27 = 20 holding
+ *         64 rows (m <= 64).
  * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
  * call (the conditions in parentheses).
  */
-#define EXL3_TEST_TILE_SHAPES 27
+#define EXL3_TEST_TILE_SHAPES 28
 exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
                                    const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                    const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,

@@ -8,7 +8,7 @@ from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
 (N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
- N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16, T128K4X64, T128X64, T128X128) = range(27)
+ N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16, T128K4X64, T128X64, T128X128, S96K4X64) = range(28)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -20,7 +20,7 @@ def plan(m, k, n, cols=None, split=False):
     # 96 column blocks: 96-column strips on 128 SMs, the decoded weights as
     # the tensor core's 128-row operand, 16-row tiles up to 16 rows
     (1, (S96K4X16, -1, 0, 0, 0)), (16, (S96K4X16, -1, 0, 0, 0)), (32, (S96K4, -1, 0, 0, 0)),
-    (48, (N96M64K4, -1, 0, 0, 0)), (64, (N96M64K4, -1, 0, 0, 0)),  # 64-row strips, four atoms a stage
+    (48, (S96K4X64, -1, 0, 0, 0)), (64, (S96K4X64, -1, 0, 0, 0)),  # 64-row swapped strips, four atoms a stage
     (128, (N96, -1, 0, 0, 0)), (256, (N96R2, -1, 0, 0, 0)),
     (512, (N256R2P, -1, 0, 0, 0)),  # 96 pair CTAs: one partial wave, nothing to split off
     (1024, (N256R2P, N128R2P, 76, 512, 7168)),  # 192 = 152 + 40 CTAs: the 40 become 40 pairs of 256x128 tiles
