@@ -297,7 +297,8 @@ def gemm(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tens
 def gemm_splitk(xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor,
                 shard_cols: Sequence[int], acc: torch.Tensor, out_dtype=torch.bfloat16,
                 out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """Split-k variant; ``acc`` is a zeroed fp32 workspace of at least splitk_workspace_bytes."""
+    """Split-k variant; ``acc`` is an fp32 workspace of at least splitk_workspace_bytes (any contents;
+    the call leaves it zeroed)."""
     m, k, n, cols, ns, cbid, out = _gemm_common(xh, trellis, bits, cb, svh, shard_cols, out_dtype, out)
     _need(acc, torch.float32, "acc")
     st = lib().exl3_gemm_splitk(_ptr(xh), m, k, _ptr(trellis), bits, cbid, _ptr(svh), cols, ns, _ptr(out),
