@@ -101,6 +101,15 @@ struct TcCfg {
   static constexpr int kRingBytes = kTRing + kNT * kTSlot;
   static constexpr int kSmem = 1024 + kCtrlBytes + kRingBytes;
   static constexpr int kMmaHalves = (BN + 127) / 128;  // SWAP: M = 128 instructions per k16 step
+  // Unswapped tiles holding at most 64 batch rows use the 64-row MMA: it reads
+  // half the activation operand of a 128-row one, most of which would be
+  // padding.  Its accumulator puts row r in tensor-memory lane
+  // (r % 16) + 32 (r / 16): lanes 32q..32q+15 of quarter q hold rows
+  // 16q..16q+15.  Measured on GB300 at m <= 32: 32-column strips 4-7% faster
+  // (12288 x 4096, 2048 x 4096, 5120 x 12288), 64-column strips on two k atoms
+  // 9% faster, 32-row grouped-expert tiles 1%; 64-column strips on four atoms
+  // neutral to 3% slower (17408 x 5120), so they keep the 128-row MMA.
+  static constexpr int kMmaM = (!SWAP && XR <= 64 && RG == 1 && !(BN == 64 && KA == 4)) ? 64 : 128;
   static constexpr int kAccCols = SWAP ? kMmaHalves * XR : RG * BN;
   static constexpr int kTmemCols =
       kAccCols <= 32 ? 32 : kAccCols <= 64 ? 64 : kAccCols <= 128 ? 128 : kAccCols <= 256 ? 256 : 512;
@@ -140,7 +149,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr int NX = C::kNX;
   constexpr int NW = C::kNW;
   constexpr int CLX = C::kClusterX;
-  constexpr uint32_t kIdesc = SWAP ? idesc_f16_f32(128, XR) : idesc_f16_f32(128, BN);
+  constexpr uint32_t kIdesc = SWAP ? idesc_f16_f32(128, XR) : idesc_f16_f32(C::kMmaM, BN);
+  // the row of the row group that a lane of accumulator quarter q holds (-1: none)
+  constexpr int kRowsPerQuarter = C::kMmaM / 4;
   static_assert(!(SWAP && MOE), "the grouped GEMM keeps the activations as the A operand");
   const GemmArgs& a = p.a;
   static_assert(!MOE || (RG == 1 && PAIR == 1 && (BN == 128 || BN == 96)),
@@ -629,8 +640,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             uint32_t q[32];
             tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
             tmem_ld_wait();
-            const int64_t row = row0 + r * 128 + quarter * 32 + lane;
-            if (ok && row < row_end) {
+            const int64_t row = row0 + r * 128 + quarter * kRowsPerQuarter + lane;
+            if (ok && lane < kRowsPerQuarter && row < row_end) {
               float4* o = reinterpret_cast<float4*>(dst + row * a.n + c0 + cc * 32);
   #pragma unroll
               for (int i = 0; i < 8; ++i)
@@ -649,7 +660,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // chunk), so only the stride-32 and stride-64 stages remain.
         if (warp >= kTcFirstDecoder) {
           const int quarter = warp & 3;
-          const bool live = row0 + r * 128 + quarter * 32 < row_end;  // this quarter holds stored rows
+          const bool live = row0 + r * 128 + quarter * kRowsPerQuarter < row_end;  // this quarter holds stored rows
           for (int cc = dw >> 2; live && cc < BN / 32; cc += kTcDecodeWarps / 4) {
             uint32_t q[32];
             tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(r * BN + cc * 32), q);
@@ -658,9 +669,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(q[e]);
             fwht32_regs(v);
-            float* dst = zs + (quarter * 32 + lane) * kZ + cc * 32;
+            float* dst = zs + (quarter * kRowsPerQuarter + lane) * kZ + cc * 32;
+            if (lane < kRowsPerQuarter) {  // with the 64-row MMA, lanes 16..31 of a quarter hold no row
   #pragma unroll
-            for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+              for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4*>(dst + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+            }
           }
         }
         if (CLX > 1) {
