@@ -887,14 +887,15 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
   }
 }
 
-// Grouped GEMM tiles: 32-row blocks on the small-batch tile (128 columns with
-// two or four k atoms per stage, or 96-column strips in clusters of four),
-// 128-row blocks on the 128-row tile.
+// Grouped GEMM tiles: 16- and 32-row blocks on the persistent tensor-memory
+// kernel (one item per row block and 128-column block), 128-row blocks on the
+// 128-row tile.
 template <int BITS, int CB>
 cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int tile, cudaStream_t stream) {
-  if (tile == kMoeTile32) return launch_tc_variant<BITS, CB, 128, 1, 2, 32, 1, true>(maps, p, stream);
-  if (tile == kMoeTile32K4) return launch_tc_variant<BITS, CB, 128, 1, 4, 32, 1, true>(maps, p, stream);
-  if (tile == kMoeTile32K4N96) return launch_tc_variant<BITS, CB, 96, 1, 4, 32, 1, true>(maps, p, stream);
+  if (tile == kMoeTileTm16K4) return launch_tm_variant<BITS, CB, 4, 16, true>(maps, p, stream);
+  if (tile == kMoeTileTm16) return launch_tm_variant<BITS, CB, 2, 16, true>(maps, p, stream);
+  if (tile == kMoeTileTm32K4) return launch_tm_variant<BITS, CB, 4, 32, true>(maps, p, stream);
+  if (tile == kMoeTileTm32) return launch_tm_variant<BITS, CB, 2, 32, true>(maps, p, stream);
   return launch_tc_variant<BITS, CB, 128, 1, 2, 128, 1, true>(maps, p, stream);
 }
 

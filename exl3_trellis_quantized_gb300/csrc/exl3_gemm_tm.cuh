@@ -152,35 +152,57 @@ __device__ __forceinline__ void decode_column(const uint32_t* w, uint32_t off, c
 }
 
 // The work item w of a call: its 128-column block, its k part, the first
-// column and the first 64-wide k atom and stage count of the part.
+// column and the first 64-wide k atom and stage count of the part; for the
+// grouped GEMM also its row block, that block's first row and expert, and
+// whether the block has an expert at all (live).
 struct TmItem {
   int64_t c0;
   int64_t kb0;
+  int64_t row0;
   int nk;
   int part;
+  int expert;
+  bool live;
 };
-template <int KA>
+template <int KA, bool MOE>
 __device__ __forceinline__ TmItem tm_item(const GemmArgs& a, int64_t w64) {
-  // 32-bit index arithmetic (every warp calls this once per item): k and n are
-  // at most 2^31, so k/128 and n/128 are at most 2^24, and there are at most
-  // 16 parts, so every product below stays under 2^28
-  const uint32_t nblk = (uint32_t)((a.n - a.col_base) >> 7);
-  const uint32_t kblk = (uint32_t)(a.k >> 7);
-  const uint32_t parts = (uint32_t)a.parts;
-  const uint32_t w = (uint32_t)w64;
-  const uint32_t part = w / nblk;
   TmItem t;
-  t.c0 = a.col_base + (int64_t)(w - part * nblk) * 128;
-  t.part = (int)part;
-  // whole 128-row blocks of k per part
-  const uint32_t kb0 = part * kblk / parts * 2;
-  const uint32_t kb1 = (part + 1) * kblk / parts * 2;
-  t.kb0 = (int64_t)kb0;
-  t.nk = (int)((kb1 - kb0) / KA);  // the host keeps KA a divisor of every part
-  return t;
+  if constexpr (MOE) {
+    // items are (row block, 128-column block), row block major
+    const int64_t nblk = a.n >> 7;
+    const int64_t blk = w64 / nblk;
+    t.c0 = (w64 - blk * nblk) * 128;
+    t.part = 0;
+    t.kb0 = 0;
+    t.nk = (int)((a.k >> 7) * 2 / KA);
+    t.row0 = blk * a.moe_block;
+    t.expert = a.block_expert[blk];
+    t.live = t.expert >= 0 && t.expert < a.num_experts;
+    return t;
+  } else {
+    // 32-bit index arithmetic (every warp calls this once per item): k and n
+    // are at most 2^31, so k/128 and n/128 are at most 2^24, and there are at
+    // most 16 parts, so every product below stays under 2^28
+    const uint32_t nblk = (uint32_t)((a.n - a.col_base) >> 7);
+    const uint32_t kblk = (uint32_t)(a.k >> 7);
+    const uint32_t parts = (uint32_t)a.parts;
+    const uint32_t w = (uint32_t)w64;
+    const uint32_t part = w / nblk;
+    t.c0 = a.col_base + (int64_t)(w - part * nblk) * 128;
+    t.part = (int)part;
+    // whole 128-row blocks of k per part
+    const uint32_t kb0 = part * kblk / parts * 2;
+    const uint32_t kb1 = (part + 1) * kblk / parts * 2;
+    t.kb0 = (int64_t)kb0;
+    t.nk = (int)((kb1 - kb0) / KA);  // the host keeps KA a divisor of every part
+    t.row0 = a.row_base;
+    t.expert = 0;
+    t.live = true;
+    return t;
+  }
 }
 
-template <int BITS, int CB, int KA, int XR>
+template <int BITS, int CB, int KA, int XR, bool MOE = false>
 __global__ void __launch_bounds__(kTmThreads, 1)
     gemm_tm_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   using C = TmCfg<BITS, KA, XR>;
@@ -209,7 +231,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t items = ((a.n - a.col_base) >> 7) * a.parts;
+  // grouped GEMM: every (row block, 128-column block); a block of no expert
+  // is skipped by every warp alike
+  const int64_t items = MOE ? (a.m / a.moe_block) * (a.n >> 7) : ((a.n - a.col_base) >> 7) * a.parts;
   const int64_t stride = gridDim.x;
   // this CTA's items: blockIdx.x, blockIdx.x + G, ...
   const int count = (int)((items - blockIdx.x + stride - 1) / stride);
@@ -253,7 +277,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA>(a, blockIdx.x + (int64_t)i * stride);
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+        if (!t.live) continue;
         const int nt0 = (int)(t.c0 >> 4);
         for (int it = 0; it < t.nk; ++it) {
           if (!mbar_wait(&tempty[s], ph ^ 1u)) {
@@ -261,8 +286,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
-          tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, (int)(t.kb0 + (int64_t)it * KA) * 4,
-                         &tfull[s]);
+          if constexpr (MOE) {
+            tma_tile4d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0,
+                           (int)(t.kb0 + (int64_t)it * KA) * 4, t.expert, &tfull[s]);
+          } else {
+            tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0,
+                           (int)(t.kb0 + (int64_t)it * KA) * 4, &tfull[s]);
+          }
           if (++s == NT) {
             s = 0;
             ph ^= 1u;
@@ -283,7 +313,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       uint32_t ph = 0;
       bool ok = true;
       for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA>(a, blockIdx.x + (int64_t)i * stride);
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+        if (!t.live) continue;
         int shard = 0;
 #pragma unroll
         for (int j = 1; j < kMaxShards; ++j)
@@ -294,7 +325,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&xfull[s], tx);
-          tma_tile4d_g2s(rings + C::kXRing + s * C::kXSlot, &maps.xh, 0, (int)a.row_base, (int)(t.kb0 + (int64_t)it * KA),
+          tma_tile4d_g2s(rings + C::kXRing + s * C::kXSlot, &maps.xh, 0, (int)t.row0, (int)(t.kb0 + (int64_t)it * KA),
                          shard, &xfull[s]);
           if (++s == NX) {
             s = 0;
@@ -316,11 +347,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       int xs = 0, as = 0;
       uint32_t xph = 0, aph = 0;
       const uint64_t xdesc0 = sdesc_sw128(smem_u32(rings + C::kXRing));
+      int li = 0;  // live items so far: they alternate the accumulator buffers
       for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA>(a, blockIdx.x + (int64_t)i * stride);
-        const int buf = i & 1;
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+        if (!t.live) continue;
+        const int buf = li & 1;
         // (every lane waits; the vote keeps the warp's decision uniform)
-        if (i >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&accempty[buf], (uint32_t)((i >> 1) - 1) & 1u))) {
+        if (li >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&accempty[buf], (uint32_t)((li >> 1) - 1) & 1u))) {
           ok = false;
           break;
         }
@@ -357,6 +390,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         }
         if (ok && leader) tc_commit(&accfull[buf]);
         __syncwarp();
+        ++li;
       }
       if (!ok && leader) *failed = 1u;
     }
@@ -395,7 +429,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     uint32_t tph = 0, aph = 0;
     bool ok = true;
     for (int i = 0; ok && i < count; ++i) {
-      const int nk = tm_item<KA>(a, blockIdx.x + (int64_t)i * stride).nk;
+      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+      if (!t.live) continue;
+      const int nk = t.nk;
       for (int it = 0; it < nk; ++it) {
         if (!mbar_wait(&tfull[ts], tph) || !mbar_wait(&aempty[as], aph ^ 1u)) {
           ok = false;
@@ -453,18 +489,24 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     // scale and store four adjacent outputs per lane.
     const int e = warp - kTmFirstEpilogue;
     const bool bf16 = a.y_bf16 != 0;
-    const int64_t live = a.m - a.row_base < XR ? a.m - a.row_base : XR;
+    // rows stored: a grouped block owns exactly its rows (padding rows of a
+    // live block included); otherwise every held row below m
+    const int64_t live =
+        MOE ? (int64_t)a.moe_block : (a.m - a.row_base < XR ? a.m - a.row_base : XR);
     uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
     float* zs = reinterpret_cast<float*>(rings + C::kZRing);
     constexpr int kZ = C::kZStride;
+    int li = 0;  // live items so far (accumulator buffer and staging phases)
     for (int i = 0; i < count; ++i) {
-      const TmItem t = tm_item<KA>(a, blockIdx.x + (int64_t)i * stride);
-      const int buf = i & 1;
+      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+      if (!t.live) continue;
+      const int buf = li & 1;
+      const uint16_t* svh = MOE ? a.svh + (int64_t)t.expert * a.n : a.svh;
       uint2 sv = make_uint2(0u, 0u);
-      if (a.parts == 1) sv = *reinterpret_cast<const uint2*>(a.svh + t.c0 + 4 * lane);
+      if (a.parts == 1) sv = *reinterpret_cast<const uint2*>(svh + t.c0 + 4 * lane);
       // every wait here is bounded: a warp that gives up leaves, and the others
       // then give up on their next wait instead of hanging
-      if (!mbar_wait(&accfull[buf], (uint32_t)(i >> 1) & 1u)) break;
+      if (!mbar_wait(&accfull[buf], (uint32_t)(li >> 1) & 1u)) break;
       tc_fence_after();
       const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
       const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
@@ -488,11 +530,11 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           float* dst = a.acc + (int64_t)t.part * a.m * a.n + t.c0 + 32 * e + lane;
 #pragma unroll
           for (int r = 0; r < ZR; ++r)
-            if (r0 + r < live) dst[(a.row_base + r0 + r) * a.n] = __uint_as_float(q[r]);
+            if (r0 + r < live) dst[(t.row0 + r0 + r) * a.n] = __uint_as_float(q[r]);
         } else {
           // staging-tile use number z of this CTA: the previous use's rows have
           // been read before the tile is rewritten
-          const uint32_t z = (uint32_t)i * (uint32_t)C::kZChunks + (uint32_t)c;
+          const uint32_t z = (uint32_t)li * (uint32_t)C::kZChunks + (uint32_t)c;
           if (z > 0 && !mbar_wait(zdone, (z - 1u) & 1u)) {
             ok = false;
             break;
@@ -511,7 +553,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             fwht128_warp(v, lane);
             const uint32_t o0 = f32_to_out((v[0] * 0.125f) * s01.x, bf16), o1 = f32_to_out((v[1] * 0.125f) * s01.y, bf16);
             const uint32_t o2 = f32_to_out((v[2] * 0.125f) * s23.x, bf16), o3 = f32_to_out((v[3] * 0.125f) * s23.y, bf16);
-            *reinterpret_cast<uint2*>(y + (a.row_base + r0 + rr) * a.n + t.c0 + 4 * lane) =
+            *reinterpret_cast<uint2*>(y + (t.row0 + r0 + rr) * a.n + t.c0 + 4 * lane) =
                 make_uint2(o0 | (o1 << 16), o2 | (o3 << 16));
           }
           // the staging tile is rewritten by the next chunk or item
@@ -520,6 +562,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         }
       }
       if (!ok) break;
+      ++li;
     }
   }
   tc_fence_before();
@@ -527,10 +570,10 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <int BITS, int CB, int KA, int XR>
+template <int BITS, int CB, int KA, int XR, bool MOE = false>
 cudaError_t launch_tm_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
   using C = TmCfg<BITS, KA, XR>;
-  auto kern = gemm_tm_kernel<BITS, CB, KA, XR>;
+  auto kern = gemm_tm_kernel<BITS, CB, KA, XR, MOE>;
   // the shared-memory opt-in and the SM count, once per device (benign race:
   // every thread writes the same values)
   static bool configured[64] = {};
@@ -546,7 +589,8 @@ cudaError_t launch_tm_variant(const TcMaps& maps, const TcParams& p, cudaStream_
     sms[dev] = v > 0 ? v : 1;
     configured[dev] = true;
   }
-  const int64_t items = ((p.a.n - p.a.col_base) >> 7) * p.a.parts;
+  const int64_t items =
+      MOE ? (p.a.m / p.a.moe_block) * (p.a.n >> 7) : ((p.a.n - p.a.col_base) >> 7) * p.a.parts;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(items < sms[dev] ? items : sms[dev]), 1u, 1u);
   cfg.blockDim = dim3(kTmThreads, 1, 1);
