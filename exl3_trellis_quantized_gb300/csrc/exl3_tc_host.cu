@@ -598,9 +598,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, int bits, int cb, cudaStream_t str
 cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  // every grouped tile holds several k atoms per stage, so a copy brings every
-  // row of the tile's region (a 16-row block rides on the 32-row tile: its
-  // second 16 rows are the next block's or zero fill, computed and not stored)
+  // each activation copy brings the block's rows (all of them: every grouped
+  // tile holds its block exactly)
   // 16- and 32-row blocks: the persistent tensor-memory kernel over (row
   // block, 128-column block) items, holding exactly the block's rows, four k
   // atoms a stage when k holds an even number of 128-blocks (measured on
