@@ -137,11 +137,7 @@ struct TcCfg {
   static_assert((2 * kNT + 2 * kNX + 3 * kNW + 1) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
 
-// MOE: grouped GEMM over row blocks of a.moe_block rows (at most XR, one row
-// group), each with its own expert: blockIdx.y is the block,
-// a.block_expert[block] the expert (the trellis map then has the experts as a
-// fourth dimension and svh is [E][n]).
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool MOE = false, bool SWAP = false>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR, bool SWAP = false>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   using C = TcCfg<BITS, BN, RG, KA, XR, PAIR, SWAP>;
@@ -152,18 +148,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t kIdesc = SWAP ? idesc_f16_f32(128, XR) : idesc_f16_f32(C::kMmaM, BN);
   // the row of the row group that a lane of accumulator quarter q holds (-1: none)
   constexpr int kRowsPerQuarter = C::kMmaM / 4;
-  static_assert(!(SWAP && MOE), "the grouped GEMM keeps the activations as the A operand");
   const GemmArgs& a = p.a;
-  static_assert(!MOE || (RG == 1 && PAIR == 1 && (BN == 128 || BN == 96)),
-                "grouped GEMM: one row group per block, 128 columns or 96-column strips");
-  // grouped GEMM: a block of no expert (-1, or an id past the last expert) is
-  // skipped; the whole CTA leaves before it touches anything
-  int expert = 0;
-  if constexpr (MOE) {
-    expert = a.block_expert[blockIdx.y];
-    if (expert < 0 || expert >= a.num_experts) return;
-  }
-  const uint16_t* const svh = MOE ? a.svh + (int64_t)expert * a.n : a.svh;
+  const uint16_t* const svh = a.svh;
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived from smem_raw by pointer arithmetic so that
@@ -195,7 +181,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     row0 = a.row_base + (rp * 2 + prank) * (128 * RG);
   } else {
     c0 = a.col_base + (int64_t)blockIdx.x * BN;
-    row0 = MOE ? (int64_t)blockIdx.y * a.moe_block : a.row_base + (int64_t)blockIdx.y * (128 * RG);
+    row0 = a.row_base + (int64_t)blockIdx.y * (128 * RG);
   }
   const int part = (int)blockIdx.z;
   // this CTA's k range in 64-wide atoms: whole 128-row blocks of k per part
@@ -252,11 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!mbar_wait(&tempty[s], ph ^ 1u)) break;
         mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);  // first 64-wide k atom of the stage
-        if constexpr (MOE) {
-          tma_tile4d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, expert, &tfull[s]);
-        } else {
-          tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, &tfull[s]);
-        }
+        tma_tile3d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0, atom0 * 4, &tfull[s]);
         if (++s == NT) {
           s = 0;
           ph ^= 1u;
@@ -556,9 +538,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
   }
   const bool bf16 = a.y_bf16 != 0;
-  // rows this CTA stores: a grouped block owns exactly its XR rows (the rows
-  // after it belong to other blocks); otherwise everything below m
-  const int64_t row_end = MOE ? row0 + a.moe_block : a.m;
+  // rows this CTA stores: everything below m
+  const int64_t row_end = a.m;
   uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
   float* zs = reinterpret_cast<float*>(rings);
   constexpr int kZ = C::kZStride;
@@ -803,10 +784,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool MOE = false, bool SWAP = false>
+template <int BITS, int CB, int BN, int RG, int KA, int XR, int PAIR = 1, bool SWAP = false>
 cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_t stream) {
   using C = TcCfg<BITS, BN, RG, KA, XR, PAIR, SWAP>;
-  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, MOE, SWAP>;
+  auto kern = gemm_tc_kernel<BITS, CB, BN, RG, KA, XR, PAIR, SWAP>;
   // the shared-memory opt-in, once per device (benign race: every thread sets
   // the same attribute)
   static bool configured[64] = {};
@@ -822,7 +803,7 @@ cudaError_t launch_tc_variant(const TcMaps& maps, const TcParams& p, cudaStream_
   if (PAIR > 1) {
     cfg.gridDim = dim3((unsigned)(2 * p.a.pair_tiles), 1u, (unsigned)p.a.parts);
   } else {
-    const int64_t row_blocks = MOE ? p.a.m / p.a.moe_block : (p.a.m - p.a.row_base + 128 * RG - 1) / (128 * RG);
+    const int64_t row_blocks = (p.a.m - p.a.row_base + 128 * RG - 1) / (128 * RG);
     cfg.gridDim = dim3((unsigned)((p.a.n - p.a.col_base) / BN), (unsigned)row_blocks, (unsigned)p.a.parts);
   }
   cfg.blockDim = dim3(kTcThreads, 1, 1);
@@ -865,14 +846,14 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kN32K4: return launch_tc_variant<BITS, CB, 32, 1, 4, 128>(maps, p, stream);
     case TcShape::kT128K4: return launch_tm_variant<BITS, CB, 4, 32>(maps, p, stream);
     case TcShape::kT128: return launch_tm_variant<BITS, CB, 2, 32>(maps, p, stream);
-    case TcShape::kS96K4: return launch_tc_variant<BITS, CB, 96, 1, 4, 32, 1, false, true>(maps, p, stream);
+    case TcShape::kS96K4: return launch_tc_variant<BITS, CB, 96, 1, 4, 32, 1, true>(maps, p, stream);
     case TcShape::kT128K4X16: return launch_tm_variant<BITS, CB, 4, 16>(maps, p, stream);
-    case TcShape::kS96K4X16: return launch_tc_variant<BITS, CB, 96, 1, 4, 16, 1, false, true>(maps, p, stream);
+    case TcShape::kS96K4X16: return launch_tc_variant<BITS, CB, 96, 1, 4, 16, 1, true>(maps, p, stream);
     case TcShape::kT128X16: return launch_tm_variant<BITS, CB, 2, 16>(maps, p, stream);
     case TcShape::kT128K4X64: return launch_tm_variant<BITS, CB, 4, 64>(maps, p, stream);
     case TcShape::kT128X64: return launch_tm_variant<BITS, CB, 2, 64>(maps, p, stream);
     case TcShape::kT128X128: return launch_tm_variant<BITS, CB, 2, 128>(maps, p, stream);
-    case TcShape::kS96K4X64: return launch_tc_variant<BITS, CB, 96, 1, 4, 64, 1, false, true>(maps, p, stream);
+    case TcShape::kS96K4X64: return launch_tc_variant<BITS, CB, 96, 1, 4, 64, 1, true>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
 }
@@ -887,16 +868,15 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
   }
 }
 
-// Grouped GEMM tiles: 16- and 32-row blocks on the persistent tensor-memory
-// kernel (one item per row block and 128-column block), 128-row blocks on the
-// 128-row tile.
+// Grouped GEMM tiles: the persistent tensor-memory kernel, one item per row
+// block and 128-column block, holding the block's 16, 32 or 128 rows.
 template <int BITS, int CB>
 cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int tile, cudaStream_t stream) {
   if (tile == kMoeTileTm16K4) return launch_tm_variant<BITS, CB, 4, 16, true>(maps, p, stream);
   if (tile == kMoeTileTm16) return launch_tm_variant<BITS, CB, 2, 16, true>(maps, p, stream);
   if (tile == kMoeTileTm32K4) return launch_tm_variant<BITS, CB, 4, 32, true>(maps, p, stream);
   if (tile == kMoeTileTm32) return launch_tm_variant<BITS, CB, 2, 32, true>(maps, p, stream);
-  return launch_tc_variant<BITS, CB, 128, 1, 2, 128, 1, true>(maps, p, stream);
+  return launch_tm_variant<BITS, CB, 2, 128, true>(maps, p, stream);  // kMoeTileTm128
 }
 
 template <int BITS>

@@ -151,14 +151,15 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
                                 cudaStream_t stream);
 // Grouped GEMM tiles: 32-row blocks with two or four k atoms per stage (or in
 // 96-column strips with four), 128-row blocks.
+// Grouped GEMM tiles: the persistent tensor-memory kernel over (row block,
+// 128-column block) items holding 16, 32 or 128 rows, four k atoms a stage
+// (16 and 32 rows with k/128 even) or two.
 enum MoeTile : int {
-  kMoeTile128 = 0,  // 128-row blocks: the 128 x 128 tile
-  // 16- and 32-row blocks: the persistent tensor-memory kernel over (row
-  // block, 128-column block) items, four k atoms a stage (k/128 even) or two
-  kMoeTileTm16K4 = 1,
-  kMoeTileTm16 = 2,
-  kMoeTileTm32K4 = 3,
-  kMoeTileTm32 = 4,
+  kMoeTileTm16K4 = 0,
+  kMoeTileTm16 = 1,
+  kMoeTileTm32K4 = 2,
+  kMoeTileTm32 = 3,
+  kMoeTileTm128 = 4,
 };
 template <int BITS>
 cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int tile, cudaStream_t stream);
