@@ -265,8 +265,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int atom0 = (int)(kb0 + (int64_t)it * KA);
         uint8_t* o = rings + C::kXRing + s * C::kXSlot;
 #pragma unroll
-        for (int r = 0; r < RG; ++r)
-          tma_tile4d_g2s(o + r * KA * C::kXAtom, &maps.xh, 0, (int)(row0 + r * 128), atom0, shard, &xfull[s]);
+        for (int r = 0; r < RG; ++r) {
+          if (KA == 1 || p.box_rows == XR) {
+            tma_tile4d_g2s(o + r * KA * C::kXAtom, &maps.xh, 0, (int)(row0 + r * 128), atom0, shard, &xfull[s]);
+          } else {
+            // fewer rows than an atom region holds: one copy per atom (the
+            // map's box is one atom), the rows past box_rows left unwritten
+#pragma unroll
+            for (int at = 0; at < KA; ++at)
+              tma_tile4d_g2s(o + (r * KA + at) * C::kXAtom, &maps.xh, 0, (int)(row0 + r * 128), atom0 + at, shard,
+                             &xfull[s]);
+          }
+        }
         if (++s == NX) {
           s = 0;
           ph ^= 1u;

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   const int64_t items = MOE ? (a.m / a.moe_block) * (a.n >> 7) : ((a.n - a.col_base) >> 7) * a.parts;
   const int64_t stride = gridDim.x;
   // this CTA's items: blockIdx.x, blockIdx.x + G, ...
-  const int count = (int)((items - blockIdx.x + stride - 1) / stride);
+  const int64_t count = (items - blockIdx.x + stride - 1) / stride;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NT; ++s) {
@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+      for (int64_t i = 0; ok && i < count; ++i) {
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
         if (!t.live) continue;
         const int nt0 = (int)(t.c0 >> 4);
         for (int it = 0; it < t.nk; ++it) {
@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
-      for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+      for (int64_t i = 0; ok && i < count; ++i) {
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
         if (!t.live) continue;
         int shard = 0;
 #pragma unroll
@@ -325,8 +325,17 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&xfull[s], tx);
-          tma_tile4d_g2s(rings + C::kXRing + s * C::kXSlot, &maps.xh, 0, (int)t.row0, (int)(t.kb0 + (int64_t)it * KA),
-                         shard, &xfull[s]);
+          const int atom0 = (int)(t.kb0 + (int64_t)it * KA);
+          if (p.box_rows == XR) {
+            tma_tile4d_g2s(rings + C::kXRing + s * C::kXSlot, &maps.xh, 0, (int)t.row0, atom0, shard, &xfull[s]);
+          } else {
+            // fewer rows than a slot's atom holds: one copy per atom (the
+            // map's box is one atom), the rows past box_rows left unwritten
+#pragma unroll
+            for (int at = 0; at < KA; ++at)
+              tma_tile4d_g2s(rings + C::kXRing + s * C::kXSlot + at * XR * 128, &maps.xh, 0, (int)t.row0, atom0 + at,
+                             shard, &xfull[s]);
+          }
           if (++s == NX) {
             s = 0;
             ph ^= 1u;
@@ -347,13 +356,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       int xs = 0, as = 0;
       uint32_t xph = 0, aph = 0;
       const uint64_t xdesc0 = sdesc_sw128(smem_u32(rings + C::kXRing));
-      int li = 0;  // live items so far: they alternate the accumulator buffers
-      for (int i = 0; ok && i < count; ++i) {
-        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+      uint32_t li = 0;  // live items so far: they alternate the accumulator buffers
+      for (int64_t i = 0; ok && i < count; ++i) {
+        const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
         if (!t.live) continue;
-        const int buf = li & 1;
+        const int buf = (int)(li & 1u);
         // (every lane waits; the vote keeps the warp's decision uniform)
-        if (li >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&accempty[buf], (uint32_t)((li >> 1) - 1) & 1u))) {
+        if (li >= 2 && !__all_sync(0xFFFFFFFFu, mbar_wait(&accempty[buf], ((li >> 1) - 1) & 1u))) {
           ok = false;
           break;
         }
@@ -428,8 +437,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     int ts = 0, as = 0;
     uint32_t tph = 0, aph = 0;
     bool ok = true;
-    for (int i = 0; ok && i < count; ++i) {
-      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+    for (int64_t i = 0; ok && i < count; ++i) {
+      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
       if (!t.live) continue;
       const int nk = t.nk;
       for (int it = 0; it < nk; ++it) {
@@ -496,17 +505,17 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     uint16_t* y = reinterpret_cast<uint16_t*>(a.y);
     float* zs = reinterpret_cast<float*>(rings + C::kZRing);
     constexpr int kZ = C::kZStride;
-    int li = 0;  // live items so far (accumulator buffer and staging phases)
-    for (int i = 0; i < count; ++i) {
-      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + (int64_t)i * stride);
+    uint32_t li = 0;  // live items so far (accumulator buffer and staging phases)
+    for (int64_t i = 0; i < count; ++i) {
+      const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
       if (!t.live) continue;
-      const int buf = li & 1;
+      const int buf = (int)(li & 1u);
       const uint16_t* svh = MOE ? a.svh + (int64_t)t.expert * a.n : a.svh;
       uint2 sv = make_uint2(0u, 0u);
       if (a.parts == 1) sv = *reinterpret_cast<const uint2*>(svh + t.c0 + 4 * lane);
       // every wait here is bounded: a warp that gives up leaves, and the others
       // then give up on their next wait instead of hanging
-      if (!mbar_wait(&accfull[buf], (uint32_t)(li >> 1) & 1u)) break;
+      if (!mbar_wait(&accfull[buf], (li >> 1) & 1u)) break;
       tc_fence_after();
       const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
       const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));
@@ -534,7 +543,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         } else {
           // staging-tile use number z of this CTA: the previous use's rows have
           // been read before the tile is rewritten
-          const uint32_t z = (uint32_t)li * (uint32_t)C::kZChunks + (uint32_t)c;
+          const uint32_t z = li * (uint32_t)C::kZChunks + (uint32_t)c;
           if (z > 0 && !mbar_wait(zdone, (z - 1u) & 1u)) {
             ok = false;
             break;

@@ -85,7 +85,7 @@ struct TcParams {
 };
 // The tensor maps one tcgen05 launch reads through.
 struct TcMaps {
-  CUtensorMap xh;       // fp16 xh, 4-D {64, m, k/64, S}: KA atoms of box_rows rows per copy
+  CUtensorMap xh;       // fp16 xh, 4-D {64, m, k/64, S}: KA atoms (1 when box_rows < XR) of box_rows rows per copy
   CUtensorMap trellis;  // int16 trellis, 3-D {16*bits, n/16, k/16}: a stage's tile rows per copy
 };
 // Tile shapes of the tcgen05 GEMM: columns per CTA (BN), row groups of 128
