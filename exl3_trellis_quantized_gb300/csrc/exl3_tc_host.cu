@@ -177,6 +177,10 @@ constexpr double kCost32K4 = 0.3;
 // parts, m = 1 to 128).
 constexpr double kCost256Split = 1.75;
 
+// Split-k at 33 to 128 rows takes the tensor-memory kernel when each CTA's
+// items hold at least this much k in all.
+constexpr int64_t kTmSplitDepth = 1024;
+
 // SMs of the current device, read once per device.
 int64_t sm_count() {
   static std::mutex mu;
@@ -291,6 +295,19 @@ TailPlan plan_tail(const GemmArgs& a, TcShape shape) {
 TcShape choose_shape(const GemmArgs& a) {
   const bool edges256 = edges_multiple_of(a, 256);
   if (a.parts > 1 && a.m <= 128) {
+    // The tensor-memory kernel over (128-column block, k part) items.  Forced
+    // shapes, whole split-k calls on GB300 (seven layers from 1024 x 512 to
+    // 17408 x 5120, 3 to 16 parts): at m <= 32 it led or tied every layer,
+    // by up to 16%; at 33-128 rows it wins where a CTA's items hold at least
+    // 1024 k in all (4-10% on 5120 x 6144, 12288 x 4096, 17408 x 5120) and
+    // loses below that (4-15% on 2048 x 4096 and smaller), where its longer
+    // prologue is not amortised.
+    const int64_t items = a.n / 128 * a.parts;
+    const int64_t sms = sm_count();
+    const int64_t depth = (items + sms - 1) / sms * (a.k / a.parts);
+    if (a.m <= 32 || depth >= kTmSplitDepth)
+      return a.m <= 16 ? TcShape::kT128X16 : a.m <= 32 ? TcShape::kT128 : a.m <= 64 ? TcShape::kT128X64
+                                                                          : TcShape::kT128X128;
     // whole waves of 128-column CTAs against fewer, wider ones
     if (edges256 && large_batch_time(a.n / 256 * a.parts, kCost256Split) < large_batch_time(a.n / 128 * a.parts, 1.0))
       return TcShape::kN256R2;
