@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // trellis, svh) is weights, which no kernel of this library writes.
       pdl_wait();
       // a split launch's tail may now be scheduled onto SMs as they free up
-      if (a.trigger_dependents) pdl_launch_dependents();
+      if (a.trigger_dependents == 1) pdl_launch_dependents();
       const uint32_t tx = (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
       int s = 0;
       uint32_t ph = 0;
@@ -533,6 +533,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp >= kTcFirstDecoder) {
     ok = mbar_wait(accfull, 0) && *failed == 0u;
+    // the split-k epilogue may be scheduled once every CTA is this far
+    if (a.trigger_dependents == 2 && warp == kTcFirstDecoder && lane == 0) pdl_launch_dependents();
     if (PAIR > 1) {
       // This CTA's copies of its decoded halves into the partner read the
       // operand ring, which the epilogue below overwrites: they are complete

@@ -516,6 +516,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       // every wait here is bounded: a warp that gives up leaves, and the others
       // then give up on their next wait instead of hanging
       if (!mbar_wait(&accfull[buf], (li >> 1) & 1u)) break;
+      // the split-k epilogue may be scheduled once every CTA has begun the
+      // epilogue of its last item
+      if (a.trigger_dependents == 2 && i + 1 == count && e == 0 && lane == 0) pdl_launch_dependents();
       tc_fence_after();
       const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sv.x));
       const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sv.y));

@@ -1,6 +1,7 @@
 // exl3_kernels_misc.cu -- the split-k epilogue, the MoE combine and the test-only decode kernels.
 #include "exl3_device.cuh"
 #include "exl3_launch.h"
+#include "exl3_sm100.cuh"
 
 namespace exl3 {
 
@@ -9,9 +10,14 @@ namespace exl3 {
 // TensorFold PR #740, "Arithmetic": parts are summed in a fixed part order).  One warp per (row, 128-column block); lane l owns
 // columns 4l..4l+3 of the block: z = ((p0 + p1) + p2) + ..., then the same
 // butterfly, scale and rounding as the fused epilogue, then zeros written back.
-// P is a template argument, so a thread holds exactly P partials.
+// P is a template argument, so a thread holds exactly P partials.  When the
+// parts' GEMM triggers it (a.trigger_dependents == 2) it is launched as a
+// programmatic dependent of that GEMM, scheduled before the GEMM ends: then
+// nothing is read or written before the GEMM has completed (pdl_wait, which
+// returns at once after a plain launch).
 template <int P>
 __global__ void __launch_bounds__(256) splitk_epilogue_kernel(const GemmArgs a) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t cb = a.n >> 7;
   const int64_t units = a.m * cb;
@@ -60,16 +66,27 @@ cudaError_t launch_splitk_epilogue(const GemmArgs& a, cudaStream_t stream) {
   const int64_t units = a.m * (a.n >> 7);
   const int64_t want = (units + 7) / 8;
   const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  void (*kern)(const GemmArgs) = nullptr;
   switch (a.parts) {  // exl3_splitk_parts returns 2..16 whenever this runs
 #define EXL3_SPLITK_CASE(P) \
-  case P: splitk_epilogue_kernel<P><<<blocks, 256, 0, stream>>>(a); break;
+  case P: kern = splitk_epilogue_kernel<P>; break;
     EXL3_SPLITK_CASE(2) EXL3_SPLITK_CASE(3) EXL3_SPLITK_CASE(4) EXL3_SPLITK_CASE(5) EXL3_SPLITK_CASE(6)
     EXL3_SPLITK_CASE(7) EXL3_SPLITK_CASE(8) EXL3_SPLITK_CASE(9) EXL3_SPLITK_CASE(10) EXL3_SPLITK_CASE(11)
     EXL3_SPLITK_CASE(12) EXL3_SPLITK_CASE(13) EXL3_SPLITK_CASE(14) EXL3_SPLITK_CASE(15) EXL3_SPLITK_CASE(16)
 #undef EXL3_SPLITK_CASE
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1u, 1u);
+  cfg.blockDim = dim3(256u, 1u, 1u);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = a.trigger_dependents == 2 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 // ---------------------------------------------------------------------------

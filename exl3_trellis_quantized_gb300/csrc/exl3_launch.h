@@ -40,8 +40,9 @@ struct GemmArgs {
   // from row_base and columns from col_base; pair shapes number their pair
   // tiles linearly, row pair major with tile_cols column tiles per row pair,
   // and launch pair_tiles of them.  trigger_dependents: let the next launch
-  // in the stream start once every CTA has its activations (the tail of a
-  // split launch, see exl3_tc_host.cu).
+  // in the stream start once every CTA has its activations (1: the tail of a
+  // split launch, see exl3_tc_host.cu) or has reached its epilogue (2: the
+  // split-k epilogue).
   int64_t row_base, col_base;
   int32_t tile_cols, pair_tiles;
   int32_t trigger_dependents;
