@@ -65,6 +65,7 @@ exl3_status_t check_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t
   a->num_shards = num_shards;
   for (int i = 0; i <= num_shards; ++i) a->shard_cols[i] = shard_cols[i];
   a->parts = 1;
+  a->part_atoms = 2;
   a->y_bf16 = (y_dtype == EXL3_BF16) ? 1 : 0;
   exl3::fill_decode_consts(&a->dc);
   return EXL3_OK;
@@ -215,6 +216,7 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
     if (acc_bytes < exl3_splitk_workspace_bytes(m, k, n)) return EXL3_EWORKSPACE;
     a.acc = acc;
     a.parts = exl3_splitk_parts(k, n);
+    a.part_atoms = exl3::split_part_atoms(k, a.parts);
   }
   if (tile_shape >= 0 && !exl3::tc_shape_supported(tile_shape, a)) return EXL3_EUNSUPPORTED;
   if (m == 0) return EXL3_OK;
@@ -262,6 +264,7 @@ exl3_status_t exl3_test_tile_plan(int64_t m, int64_t k, int64_t n, const int32_t
   a.num_shards = num_shards;
   for (int i = 0; i <= num_shards; ++i) a.shard_cols[i] = shard_cols[i];
   a.parts = split ? exl3_splitk_parts(k, n) : 1;
+  a.part_atoms = exl3::split_part_atoms(k, a.parts);
   exl3::tc_plan(a, out);
   return EXL3_OK;
 }

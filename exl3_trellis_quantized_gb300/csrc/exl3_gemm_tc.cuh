@@ -184,9 +184,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     row0 = a.row_base + (int64_t)blockIdx.y * (128 * RG);
   }
   const int part = (int)blockIdx.z;
-  // this CTA's k range in 64-wide atoms: whole 128-row blocks of k per part
-  const int64_t kb0 = (int64_t)part * (a.k >> 7) / a.parts * 2;
-  const int64_t kb1 = (int64_t)(part + 1) * (a.k >> 7) / a.parts * 2;
+  // this CTA's k range in 64-wide atoms: whole units of part_atoms atoms per
+  // part (part_atoms = 2 without a split)
+  const int64_t units = (a.k >> 6) / a.part_atoms;
+  const int64_t kb0 = (int64_t)part * units / a.parts * a.part_atoms;
+  const int64_t kb1 = (int64_t)(part + 1) * units / a.parts * a.part_atoms;
   const int nk = (int)((kb1 - kb0) / KA);  // pipeline stages (the host keeps KA a divisor of every part)
 
   int shard = 0;

@@ -181,18 +181,20 @@ __device__ __forceinline__ TmItem tm_item(const GemmArgs& a, int64_t w64) {
     return t;
   } else {
     // 32-bit index arithmetic (every warp calls this once per item): k and n
-    // are at most 2^31, so k/128 and n/128 are at most 2^24, and there are at
-    // most 16 parts, so every product below stays under 2^28
+    // are at most 2^31, so n/128 and the k units (2 or 4 atoms of 64) are at
+    // most 2^24, and there are at most 16 parts, so every product below stays
+    // under 2^28 before its scaling by part_atoms
     const uint32_t nblk = (uint32_t)((a.n - a.col_base) >> 7);
-    const uint32_t kblk = (uint32_t)(a.k >> 7);
+    const uint32_t pa = (uint32_t)a.part_atoms;
+    const uint32_t kunits = (uint32_t)(a.k >> 6) / pa;
     const uint32_t parts = (uint32_t)a.parts;
     const uint32_t w = (uint32_t)w64;
     const uint32_t part = w / nblk;
     t.c0 = a.col_base + (int64_t)(w - part * nblk) * 128;
     t.part = (int)part;
-    // whole 128-row blocks of k per part
-    const uint32_t kb0 = part * kblk / parts * 2;
-    const uint32_t kb1 = (part + 1) * kblk / parts * 2;
+    // whole units of part_atoms atoms of k per part
+    const uint32_t kb0 = part * kunits / parts * pa;
+    const uint32_t kb1 = (part + 1) * kunits / parts * pa;
     t.kb0 = (int64_t)kb0;
     t.nk = (int)((kb1 - kb0) / KA);  // the host keeps KA a divisor of every part
     t.row0 = a.row_base;

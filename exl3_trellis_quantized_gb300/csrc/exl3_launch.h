@@ -30,7 +30,8 @@ struct GemmArgs {
   int64_t m, k, n;
   int32_t shard_cols[kMaxShards + 1];
   int32_t num_shards;
-  int32_t parts;  // P (1 = no split)
+  int32_t parts;       // P (1 = no split)
+  int32_t part_atoms;  // a part is whole units of this many 64-wide k atoms (2 or 4)
   int32_t y_bf16;
   DecodeConsts dc;
   // grouped (mixture-of-experts) GEMM only: expert of each row block, or -1
@@ -48,6 +49,14 @@ struct GemmArgs {
   int32_t trigger_dependents;
   int32_t moe_block;  // grouped GEMM: rows per block (16, 32 or 128)
 };
+
+// Split-k parts are whole units of four 64-wide k atoms (256 rows of k) when
+// k/128 is even and every part gets at least one such unit, else whole
+// 128-row blocks (two atoms); like P itself a function of the shape only.
+inline int32_t split_part_atoms(int64_t k, int32_t parts) {
+  const int64_t kb = k / 128;
+  return (parts > 1 && kb % 2 == 0 && parts <= kb / 2) ? 4 : 2;
+}
 
 cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_t k, const uint16_t* suh,
                                    int num_shards, uint16_t* xh, cudaStream_t stream);

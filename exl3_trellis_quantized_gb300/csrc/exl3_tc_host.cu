@@ -305,9 +305,13 @@ TcShape choose_shape(const GemmArgs& a) {
     const int64_t items = a.n / 128 * a.parts;
     const int64_t sms = sm_count();
     const int64_t depth = (items + sms - 1) / sms * (a.k / a.parts);
-    if (a.m <= 32 || depth >= kTmSplitDepth)
+    if (a.m <= 32 || depth >= kTmSplitDepth) {
+      // four atoms a stage when the parts are whole four-atom units
+      if (a.part_atoms == 4 && a.m <= 64)
+        return a.m <= 16 ? TcShape::kT128K4X16 : a.m <= 32 ? TcShape::kT128K4 : TcShape::kT128K4X64;
       return a.m <= 16 ? TcShape::kT128X16 : a.m <= 32 ? TcShape::kT128 : a.m <= 64 ? TcShape::kT128X64
                                                                           : TcShape::kT128X128;
+    }
     // whole waves of 128-column CTAs against fewer, wider ones
     if (edges256 && large_batch_time(a.n / 256 * a.parts, kCost256Split) < large_batch_time(a.n / 128 * a.parts, 1.0))
       return TcShape::kN256R2;
@@ -431,8 +435,11 @@ bool tc_shape_supported(int shape, const GemmArgs& a) {
   // small-batch shapes hold XR rows; the tensor-memory kernel holds XR rows
   // whatever XR is (it has no row groups)
   if ((d.xr < 128 || tm_shape(s)) && a.m > d.xr) return false;
-  // several atoms per stage: k must hold whole stages, and no split-k
-  if (d.ka > 2 && ((a.k / 128) % (d.ka / 2) != 0 || a.parts > 1)) return false;
+  // several atoms per stage: k must hold whole stages, and split-k parts
+  // only the tensor-memory kernel's four-atom stages, on four-atom parts
+  if (d.ka > 2 && ((a.k / 128) % (d.ka / 2) != 0 ||
+                   (a.parts > 1 && !(tm_shape(s) && d.ka == 4 && a.part_atoms == 4))))
+    return false;
   // n and every shard edge fall on whole CTA spans: lcm(BN, 128) columns (a
   // cluster's span when BN is not a multiple of 128)
   return edges_multiple_of(a, lcm_128(d.bn));

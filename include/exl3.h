@@ -142,7 +142,10 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
  * layers: partials go to an fp32 accumulator that a second kernel turns into
  * outputs while zeroing it again); TensorFold PR #740, "Arithmetic" (k
  * blocks split into a number of parts fixed by the shape, parts added in part
- * order).  Part p covers a contiguous range of whole 128-row blocks of k; its
+ * order).  Part p covers a contiguous range of k: whole 256-row units when
+ * k/128 is even and P <= k/256 (so a part never splits a four-atom stage),
+ * else whole 128-row blocks, in either case part p takes units
+ * [p*U/P, (p+1)*U/P) of the U units; its
  * fp32 partial goes to acc[p][r][c]; the epilogue sums p = 0..P-1 in order,
  * applies the output rotation, writes y and writes zeros back to acc.
  *

@@ -287,6 +287,40 @@ def test_tensor_memory_shapes_every_width(bits, cb):
         _assert_columns(_np(want), ref[:m], f"bits={bits} cb={cb} m={m}", ref_batch=ref)
 
 
+@pytest.mark.parametrize("bits", [1, 3, 4, 6, 8])
+@pytest.mark.parametrize("cb", [0, 1, 2])
+def test_split_four_atom_parts(bits, cb):
+    """Split-k parts of whole 256-row units of k (k/128 even and P <= k/256:
+    here 1024 x 4864, 38 column blocks, P = 4): the tensor-memory kernel's
+    four-atom shapes run them and give the bytes of the shared-memory tiles'
+    parts and of its two-atom shapes, the workspace comes back zeroed, and the
+    result meets the oracle on a first, a middle and the last column block."""
+    k, n = 1024, 4864
+    assert E.splitk_parts(k, n) == 4
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=4700 + 3 * bits + cb)
+    tr, suh, svh = _dev(layer)
+    x = synthetic.make_x(64, k, seed=4701)
+    blocks = [0, 17, 37]
+    ref = _oracle(x, layer, col_blocks=blocks)
+    cols = np.concatenate([np.arange(128 * b, 128 * b + 128) for b in blocks])
+    for m in (1, 7, 16, 29, 32, 50, 64):
+        xh = E.input_transform(x[:m].to(DEV), suh)
+        acc = torch.zeros(max(1, E.splitk_workspace_bytes(m, k, n) // 4), dtype=torch.float32, device=DEV)
+        want = B.test_gemm_shape(1 if m <= 32 else 3, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+        assert want is not None
+        want = want.clone()
+        got = E.gemm_splitk(xh, tr, bits, cb, svh, layer.shard_cols, acc)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"m={m}: planned split differs"
+        for shape, rows in TM_SHAPES.items():
+            if m > rows:
+                continue
+            got = B.test_gemm_shape(shape, xh, tr, bits, cb, svh, layer.shard_cols, acc)
+            assert got is not None, f"shape {shape} refused m={m}"
+            assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"shape {shape} m={m}: bytes differ"
+            assert not bool(acc.any()), f"shape {shape} m={m}: workspace not re-zeroed"
+        _assert_columns(_np(want)[:, cols], ref[:m], f"bits={bits} cb={cb} m={m}", ref_batch=ref)
+
+
 @pytest.mark.parametrize("m", [3, 16, 29, 61, 100])
 def test_tensor_memory_kernel_many_items(m):
     """A persistent launch with several waves of work items and a ragged last

@@ -58,12 +58,15 @@ def test_narrow_and_split_layers():
     assert plan(16, 4224, 154880)[0] == T128X16  # odd k/128: two atoms a stage
     assert plan(16, 4096, 8192)[0] == N64SK4  # 64 blocks: 64-column strips, four atoms a stage
     assert plan(16, 384, 4096)[0] != N32S  # odd k/128: no four-atom tiles
-    # split-k at m <= 32: the tensor-memory kernel over (block, part) items
-    assert plan(1, 17408, 5120, split=True)[0] == T128X16  # 7 parts of 40 blocks
-    assert plan(16, 1024, 512, split=True)[0] == T128X16
-    assert plan(32, 2048, 4096, split=True)[0] == T128
+    # split-k at m <= 32: the tensor-memory kernel over (block, part) items,
+    # four atoms a stage when the parts are whole 256-row units of k (k/128
+    # even and P <= k/256), else two
+    assert plan(1, 17408, 5120, split=True)[0] == T128K4X16  # 7 parts of 68 units
+    assert plan(32, 12288, 4096, split=True)[0] == T128K4  # 9 parts of 48 units
+    assert plan(16, 1024, 512, split=True)[0] == T128X16  # 8 parts > 4 units
+    assert plan(32, 2048, 4096, split=True)[0] == T128  # 9 parts > 8 units
     # 33-128 rows: there too when a CTA's items hold >= 1024 k in all
-    assert plan(64, 17408, 5120, split=True)[0] == T128X64  # 2 waves of 2487-deep parts
+    assert plan(64, 17408, 5120, split=True)[0] == T128K4X64  # 2 waves of 2487-deep parts
     assert plan(128, 5120, 6144, split=True)[0] == T128X128  # 1 wave of 1707-deep parts
     assert plan(64, 2048, 4096, split=True)[0] == N256R2  # 2 x 228 k: shared-memory tiles
     assert plan(128, 4096, 1024, split=True)[0] == N128  # 1 x 256 k
