@@ -342,7 +342,7 @@ def linear(x: torch.Tensor, trellis: torch.Tensor, bits: int, cb, suh: torch.Ten
 
 
 # Tile shapes exl3_test_gemm_shape accepts (EXL3_TEST_TILE_SHAPES in include/exl3.h).
-TEST_TILE_SHAPES = 28
+TEST_TILE_SHAPES = 29
 
 
 def test_gemm_shape(tile_shape: int, xh: torch.Tensor, trellis: torch.Tensor, bits: int, cb, svh: torch.Tensor,

@@ -867,6 +867,7 @@ cudaError_t launch_tc_cb(const TcMaps& maps, const TcParams& p, TcShape shape, c
     case TcShape::kT128K4X64: return launch_tm_variant<BITS, CB, 4, 64>(maps, p, stream);
     case TcShape::kT128X64: return launch_tm_variant<BITS, CB, 2, 64>(maps, p, stream);
     case TcShape::kT128X128: return launch_tm_variant<BITS, CB, 2, 128>(maps, p, stream);
+    case TcShape::kT128K4X128: return launch_tm_variant<BITS, CB, tm128_k4_atoms(BITS), 128>(maps, p, stream);
     case TcShape::kS96K4X64: return launch_tc_variant<BITS, CB, 96, 1, 4, 64, 1, true>(maps, p, stream);
     default: return launch_tc_variant<BITS, CB, 256, 2, 1, 128>(maps, p, stream);
   }
@@ -890,6 +891,7 @@ cudaError_t launch_moe_cb(const TcMaps& maps, const TcParams& p, int tile, cudaS
   if (tile == kMoeTileTm16) return launch_tm_variant<BITS, CB, 2, 16, true>(maps, p, stream);
   if (tile == kMoeTileTm32K4) return launch_tm_variant<BITS, CB, 4, 32, true>(maps, p, stream);
   if (tile == kMoeTileTm32) return launch_tm_variant<BITS, CB, 2, 32, true>(maps, p, stream);
+  if (tile == kMoeTileTm128K4) return launch_tm_variant<BITS, CB, tm128_k4_atoms(BITS), 128, true>(maps, p, stream);
   return launch_tm_variant<BITS, CB, 2, 128, true>(maps, p, stream);  // kMoeTileTm128
 }
 

@@ -138,7 +138,8 @@ enum class TcShape : int {
   kT128X64,      // BN=128, KA=2, XR=64 (m <= 64)
   kT128X128,     // BN=128, KA=2, XR=128 (m <= 128)
   kS96K4X64,     // BN=96,  KA=4, XR=64 (m <= 64, k/128 even, no split-k, 384-aligned edges)
-  kLast = kS96K4X64,
+  kT128K4X128,   // BN=128, KA=4 (2 at 7-8 bits), XR=128 (m <= 128, k/128 even)
+  kLast = kT128K4X128,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
 // (parts > 1) for the split-k epilogue.
@@ -164,12 +165,19 @@ cudaError_t launch_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, T
 // Grouped GEMM tiles: the persistent tensor-memory kernel over (row block,
 // 128-column block) items holding 16, 32 or 128 rows, four k atoms a stage
 // (16 and 32 rows with k/128 even) or two.
+// Atoms a stage of the 128-row four-atom tensor-memory tiles (dense and
+// grouped): two 64 KB activation slots leave room for three trellis slots of
+// four atoms only up to 6 bits.  The host's tensor maps and the kernel's
+// instantiation both follow this.
+constexpr int tm128_k4_atoms(int bits) { return bits <= 6 ? 4 : 2; }
+
 enum MoeTile : int {
   kMoeTileTm16K4 = 0,
   kMoeTileTm16 = 1,
   kMoeTileTm32K4 = 2,
   kMoeTileTm32 = 3,
   kMoeTileTm128 = 4,
+  kMoeTileTm128K4 = 5,  // four atoms a stage (two at 7-8 bits, where three trellis slots would not fit)
 };
 template <int BITS>
 cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int tile, cudaStream_t stream);

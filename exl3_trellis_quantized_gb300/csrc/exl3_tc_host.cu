@@ -113,6 +113,7 @@ ShapeDims dims_of(TcShape s) {
     case TcShape::kT128K4X64: return {128, 4, 64, 1, 1};
     case TcShape::kT128X64: return {128, 2, 64, 1, 1};
     case TcShape::kT128X128: return {128, 2, 128, 1, 1};
+    case TcShape::kT128K4X128: return {128, 4, 128, 1, 1};  // 2 atoms at 7-8 bits (launch_one)
     case TcShape::kS96K4X64: return {96, 4, 64, 1, 1};
     default: return {256, 1, 128, 1, 2};
   }
@@ -142,8 +143,11 @@ double rel_tm(int64_t waves) { return waves <= 1 ? 1.02 : waves == 2 ? 1.06 : wa
 // 32 < m <= 64 measured at the same per-SM rates as at m <= 32 (5120 x 12288:
 // 1.03 in one wave, 5120 x 34816: 1.07 in two, 4096 x 154880: 1.41 in eight);
 // holding 128 rows on two k atoms at 64 < m <= 128, about 0.89 of them (0.91,
-// 0.94, 1.22 on the same layers).
+// 0.94, 1.22 on the same layers); on four atoms (k/128 even), about 0.92 of
+// them (4096 x 154880: 178.5 against 165 us at m = 64, 5120 x 34816: 61.8
+// against 56.5 us; 10-17% faster than on two atoms).
 constexpr double kRelTm128 = 0.89;
+constexpr double kRelTm128K4 = 0.92;
 // 256-column, 256-row tiles at 32 < m <= 128 against 128 columns, per column
 // (5120 x 34816, 4096 x 154880): fewer CTAs in whole waves.
 constexpr double kRel256Mid = 1.07;
@@ -307,8 +311,9 @@ TcShape choose_shape(const GemmArgs& a) {
     const int64_t depth = (items + sms - 1) / sms * (a.k / a.parts);
     if (a.m <= 32 || depth >= kTmSplitDepth) {
       // four atoms a stage when the parts are whole four-atom units
-      if (a.part_atoms == 4 && a.m <= 64)
-        return a.m <= 16 ? TcShape::kT128K4X16 : a.m <= 32 ? TcShape::kT128K4 : TcShape::kT128K4X64;
+      if (a.part_atoms == 4)
+        return a.m <= 16 ? TcShape::kT128K4X16 : a.m <= 32 ? TcShape::kT128K4 : a.m <= 64 ? TcShape::kT128K4X64
+                                                                             : TcShape::kT128K4X128;
       return a.m <= 16 ? TcShape::kT128X16 : a.m <= 32 ? TcShape::kT128 : a.m <= 64 ? TcShape::kT128X64
                                                                           : TcShape::kT128X128;
     }
@@ -369,9 +374,11 @@ TcShape choose_shape(const GemmArgs& a) {
     const double r32 = (a.k / 128) % 2 == 0 ? small_batch_rate(a.n / 32, kRel32Full) : 0.0;
     const int64_t sms = sm_count();
     const int64_t blocks = a.n / 128;
+    const bool k4 = (a.k / 128) % 2 == 0;
     const double rt =
-        kRelTm128 * rel_tm((blocks + sms - 1) / sms) * (double)(blocks < sms ? blocks : sms);
-    if (rt >= r128 && rt >= r256 && rt >= r96 && rt >= r64 && rt >= r32) return TcShape::kT128X128;
+        (k4 ? kRelTm128K4 : kRelTm128) * rel_tm((blocks + sms - 1) / sms) * (double)(blocks < sms ? blocks : sms);
+    if (rt >= r128 && rt >= r256 && rt >= r96 && rt >= r64 && rt >= r32)
+      return k4 ? TcShape::kT128K4X128 : TcShape::kT128X128;
     if (r256 > r128 && r256 >= r96 && r256 >= r64 && r256 >= r32) return TcShape::kN256R2;
     if (r32 > r128 && r32 > r96 && r32 > r64) return TcShape::kN32K4;
     if (r64 > r128 && r64 > r96) return TcShape::kN64K4;
@@ -425,7 +432,7 @@ void tc_plan(const GemmArgs& a, int64_t out[5]) {
 // grid over column items only.
 static bool tm_shape(TcShape s) {
   return s == TcShape::kT128K4 || s == TcShape::kT128 || s == TcShape::kT128K4X16 || s == TcShape::kT128X16 ||
-         s == TcShape::kT128K4X64 || s == TcShape::kT128X64 || s == TcShape::kT128X128;
+         s == TcShape::kT128K4X64 || s == TcShape::kT128X64 || s == TcShape::kT128X128 || s == TcShape::kT128K4X128;
 }
 
 bool tc_shape_supported(int shape, const GemmArgs& a) {
@@ -452,7 +459,8 @@ namespace {
 cudaError_t launch_one(const GemmArgs& a, int bits, int cb, TcShape shape, cudaStream_t stream) {
   TcParams p;
   p.a = a;
-  const ShapeDims d = dims_of(shape);
+  ShapeDims d = dims_of(shape);
+  if (shape == TcShape::kT128K4X128) d.ka = tm128_k4_atoms(bits);
   p.a.tile_cols = (int32_t)((a.n - a.col_base) / d.bn);
   if (d.pair > 1 && p.a.pair_tiles == 0) {
     const int64_t rows_per_tile = 2 * 128 * d.rg;
@@ -634,9 +642,11 @@ cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, c
   const bool k4 = (a.k / 128) % 2 == 0;
   const int tile = block <= 32 ? (block == 16 ? (k4 ? kMoeTileTm16K4 : kMoeTileTm16)
                                               : (k4 ? kMoeTileTm32K4 : kMoeTileTm32))
-                               : kMoeTileTm128;
+                               : (k4 ? kMoeTileTm128K4 : kMoeTileTm128);
   p.box_rows = block;
-  const int ka = (tile == kMoeTileTm16K4 || tile == kMoeTileTm32K4) ? 4 : 2;
+  const int ka = (tile == kMoeTileTm16K4 || tile == kMoeTileTm32K4) ? 4
+                 : tile == kMoeTileTm128K4                          ? tm128_k4_atoms(bits)
+                                                                    : 2;
   const int bn = 128;
   TcMaps maps;
   cudaError_t e = make_xh_map(&maps.xh, a.xh, a.m, a.k, a.num_shards, p.box_rows, ka);

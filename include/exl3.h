@@ -329,18 +329,20 @@ exl3_status_t exl3_test_unpack(const int16_t* trellis, int32_t bits, exl3_codebo
  *     The decoded weights as the tensor core's 128-row operand and the batch
  *     rows as the narrow one (18, 19, 21, 23 keep the decoded weights in
  *     tensor memory, 20 and 22 in shared memory):
- *     18 = 128 columns, four k atoms per stage (m <= 32, k/128 even, no
- *         split-k), 19 = 128 columns, two k atoms (m <= 32), 20 = 96-column
+ *     18 = 128 columns, four k atoms per stage (m <= 32, k/128 even; under
+ *         split-k only when its parts are whole 256-row units of k), 19 =
+ *         128 columns, two k atoms (m <= 32), 20 = 96-column
  *         strips in clusters of four, four k atoms (m <= 32, k/128 even, no
  *         split-k, n and shard edges multiples of 384), 21 and 22 = 18 and 20
  *         holding 16 rows (m <= 16), 23 = 19 holding 16 rows (m <= 16),
  *         24 = 18 holding 64 rows (m <= 64), 25 = 19 holding 64 rows
  *         (m <= 64), 26 = 19 holding 128 rows (m <= 128), 27 = 20 holding
- *         64 rows (m <= 64).
+ *         64 rows (m <= 64), 28 = 18 holding 128 rows (m <= 128; two k
+ *         atoms per stage at 7-8 bits).
  * Returns EXL3_EUNSUPPORTED, launching nothing, when the shape cannot run the
  * call (the conditions in parentheses).
  */
-#define EXL3_TEST_TILE_SHAPES 28
+#define EXL3_TEST_TILE_SHAPES 29
 exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64_t m, int64_t k,
                                    const int16_t* trellis, int32_t bits, exl3_codebook_t cb,
                                    const uint16_t* svh, const int32_t* shard_cols, int32_t num_shards,

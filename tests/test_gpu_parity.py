@@ -243,13 +243,13 @@ def test_every_tile_shape_byte_equal(k, widths, bits, cb, split):
     need = {1, 2, 3, 4, 6, 19, 23, 25, 26} | ({5, 7} if all(w % 256 == 0 for w in widths) else set())
     need |= {10, 11} if all(w % 384 == 0 for w in widths) else set()
     if not split and (k // 128) % 2 == 0:
-        need |= {0, 8, 13, 15, 16, 17, 18, 21, 24} | ({9, 14, 20, 22, 27} if all(w % 384 == 0 for w in widths) else set())
+        need |= {0, 8, 13, 15, 16, 17, 18, 21, 24, 28} | ({9, 14, 20, 22, 27} if all(w % 384 == 0 for w in widths) else set())
     if not split and k % 512 == 0:
         need |= {12}
     assert need <= ran, f"shapes not exercised: {sorted(need - ran)}"
 
 
-TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16, 24: 64, 25: 64, 26: 128}  # tensor-memory shapes and their rows
+TM_SHAPES = {18: 32, 19: 32, 21: 16, 23: 16, 24: 64, 25: 64, 26: 128, 28: 128}  # tensor-memory shapes and their rows
 
 
 @pytest.mark.parametrize("bits", range(1, 9))

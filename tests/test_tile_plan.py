@@ -8,7 +8,8 @@ from exl3_trellis_quantized_gb300 import binding as B
 
 SMS = 152  # the plan uses the current device's SM count, 152 without one
 (N32S, N64S, N128S, N128, N128R2, N256R2, N128R2P, N256R2P, N128SK4, N96SK4, N96, N96R2, N32SK8, N64SK4, N96M64K4,
- N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16, T128K4X64, T128X64, T128X128, S96K4X64) = range(28)
+ N64M64K4, N64K4, N32K4, T128K4, T128, S96K4, T128K4X16, S96K4X16, T128X16, T128K4X64, T128X64, T128X128, S96K4X64,
+ T128K4X128) = range(29)
 PAIR_BN = {N128R2P: 128, N256R2P: 256}
 
 
@@ -36,12 +37,12 @@ def test_q_proj_plan(m, want):
     (64, 12416, 4096, None, N128), (100, 12416, 4096, None, N128),  # odd k/128: no four-atom strips
     (64, 4096, 2048, None, N32K4),  # 16 blocks: 64 strips of 32 columns
     (128, 5120, 6144, None, N64K4), (100, 5120, 12288, None, N96),
-    # wide layers: the tensor-memory kernel holding 64 rows (four atoms) or 128
-    # rows (two atoms) where its persistent waves beat 256-column tiles
+    # wide layers: the tensor-memory kernel holding 64 or 128 rows (four atoms
+    # a stage when k/128 is even) where its persistent waves beat 256-column tiles
     (48, 5120, 34816, [0, 17408, 34816], T128K4X64), (64, 4096, 154880, None, T128K4X64),
-    (128, 4096, 154880, None, T128X128), (100, 4096, 154880, None, T128X128),
-    (128, 5120, 34816, [0, 17408, 34816], N256R2),  # two waves of items: 256-column tiles stay ahead
-    (48, 4224, 154880, None, T128X128),  # odd k/128: no four-atom tiles, the 128-row items
+    (128, 4096, 154880, None, T128K4X128), (100, 4096, 154880, None, T128K4X128),
+    (128, 5120, 34816, [0, 17408, 34816], T128K4X128),  # two waves of items, still ahead of 256-column tiles
+    (48, 4224, 154880, None, T128X128),  # odd k/128: no four-atom tiles, the 128-row items on two
 ])
 def test_mid_batch_plan(m, k, n, cols, want):
     assert plan(m, k, n, cols)[0] == want
@@ -67,7 +68,7 @@ def test_narrow_and_split_layers():
     assert plan(32, 2048, 4096, split=True)[0] == T128  # 9 parts > 8 units
     # 33-128 rows: there too when a CTA's items hold >= 1024 k in all
     assert plan(64, 17408, 5120, split=True)[0] == T128K4X64  # 2 waves of 2487-deep parts
-    assert plan(128, 5120, 6144, split=True)[0] == T128X128  # 1 wave of 1707-deep parts
+    assert plan(128, 5120, 6144, split=True)[0] == T128K4X128  # 1 wave of 1707-deep parts
     assert plan(64, 2048, 4096, split=True)[0] == N256R2  # 2 x 228 k: shared-memory tiles
     assert plan(128, 4096, 1024, split=True)[0] == N128  # 1 x 256 k
 
