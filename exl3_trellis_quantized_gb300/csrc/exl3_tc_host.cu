@@ -635,10 +635,11 @@ cudaError_t launch_moe_gemm_tc(const GemmArgs& a, int bits, int cb, int block, c
   p.a = a;
   // The persistent tensor-memory kernel over (row block, 128-column block)
   // items, holding exactly the block's rows (each activation copy brings
-  // them), four k atoms a stage for 16- and 32-row blocks when k holds an even
-  // number of 128-blocks.  Measured on 128 experts, top-8, hidden 2048,
-  // gate_up 2 x 768, 4-bit mcg: 1.2-1.4x faster than one CTA per (block,
-  // column tile) at 1 to 256 tokens, 1.1x with 128-row blocks at 1024.
+  // them), four k atoms a stage when k holds an even number of 128-blocks
+  // (128-row blocks only up to 6 bits).  Measured on 128 experts, top-8,
+  // hidden 2048, gate_up 2 x 768, 4-bit mcg: 1.2-1.4x faster than one CTA per
+  // (block, column tile) at 1 to 256 tokens, 1.1x with 128-row blocks on two
+  // atoms at 1024 tokens, and four atoms there 163 -> 151 us.
   const bool k4 = (a.k / 128) % 2 == 0;
   const int tile = block <= 32 ? (block == 16 ? (k4 ? kMoeTileTm16K4 : kMoeTileTm16)
                                               : (k4 ? kMoeTileTm32K4 : kMoeTileTm32))
