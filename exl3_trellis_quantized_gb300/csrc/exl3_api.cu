@@ -222,7 +222,7 @@ exl3_status_t exl3_test_gemm_shape(int32_t tile_shape, const uint16_t* xh, int64
   if (m == 0) return EXL3_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.parts == 1) {
-    // no split (or one part: the fused epilogue does everything; acc stays zero)
+    // no split (or one part: the fused epilogue does everything; acc untouched)
     return cuda_status(exl3::launch_gemm_tc(a, bits, cb, s, tile_shape), "exl3_gemm");
   }
   // Up to 16 rows the epilogue follows as a programmatic dependent, scheduled

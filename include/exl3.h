@@ -157,9 +157,11 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
  *              each part stores every partial it owns (plain stores, no
  *              accumulation into acc) before the epilogue reads it.  The
  *              epilogue writes zeros back, the pages' re-zeroed accumulator,
- *              so acc is all zero when the call's work completes; nothing
- *              relies on that.  Calls that share one acc must be ordered on
- *              one stream.
+ *              so with P > 1 acc is all zero when the call's work completes;
+ *              nothing relies on that.  With P = 1 the call computes what
+ *              exl3_gemm computes, with no partials and no epilogue, and
+ *              leaves acc as it found it.  Calls that share one acc must be
+ *              ordered on one stream.
  *   acc_bytes  size of acc in bytes; smaller than the workspace size -> EXL3_EWORKSPACE
  *   other arguments as exl3_gemm.
  * If a kernel of the call gives up on a bounded wait (exl3_device_status then

@@ -287,6 +287,23 @@ def test_tensor_memory_shapes_every_width(bits, cb):
         _assert_columns(_np(want), ref[:m], f"bits={bits} cb={cb} m={m}", ref_batch=ref)
 
 
+def test_splitk_one_part_is_gemm():
+    """A layer whose column blocks fill the GPU gets one part: the split-k call
+    then gives exl3_gemm's bytes and leaves the workspace as it found it (here
+    NaN-filled)."""
+    k, n, bits, cb = 256, 152 * 128, 4, 1
+    assert E.splitk_parts(k, n) == 1
+    layer = synthetic.make_layer(k, [n], bits, cb, seed=4800)
+    tr, suh, svh = _dev(layer)
+    for m in (1, 16, 100):
+        xh = E.input_transform(synthetic.make_x(m, k, seed=4801).to(DEV), suh)
+        want = E.gemm(xh, tr, bits, cb, svh, layer.shard_cols)
+        acc = torch.full((E.splitk_workspace_bytes(m, k, n) // 4,), float("nan"), dtype=torch.float32, device=DEV)
+        got = E.gemm_splitk(xh, tr, bits, cb, svh, layer.shard_cols, acc)
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), f"m={m}"
+        assert bool(torch.isnan(acc).all()), f"m={m}: workspace touched"
+
+
 @pytest.mark.parametrize("bits", [1, 3, 4, 6, 8])
 @pytest.mark.parametrize("cb", [0, 1, 2])
 def test_split_four_atom_parts(bits, cb):
