@@ -12,8 +12,7 @@
 // per pass with 16-byte loads.  Butterfly stages of stride 1..8 stay in
 // registers; for the stride-16, -32 and -64 stages the warp regroups its blocks
 // once through shared memory (rotate_store16).  The SwiGLU and grouped-expert
-// transforms give four lanes to a block (32 elements each, strides 1..16 in
-// registers, 32 and 64 after the regroup: rotate_store).
+// transforms use the same layout.
 // Each stage computes (a, b) -> (a + b, a - b) on the same pairs as the plain
 // definition, so the order of fp32 adds is the fixed one.  x is read once and reused for
 // every shard.  The kernel is HBM/L2-bound: 2 bytes in, 2*S bytes out per
@@ -35,79 +34,13 @@ __device__ __forceinline__ void unpack8(const uint4 w, uint16_t (&e)[8]) {
   }
 }
 
-// The Hadamard butterfly of a lane's 32 values, times 2^-4, rounded to fp16
+// The Hadamard butterfly of a block over eight lanes, 16 values a lane
+// (elements 16p..16p+15 of lane p of the eight), times 2^-4, rounded to fp16
 // and stored at dst (nothing is stored when dst is null; the lane still takes
-// part in the exchange).  Stages of stride 1..16 run in registers.  For the
-// stride-32 and stride-64 stages the warp's eight blocks go through its
-// shared-memory area xp (8 x 128 floats) once: each lane then holds elements
-// j, j+32, j+64, j+96 for its eight j = 8q..8q+7 and finishes both stages in
-// registers.  Every stage still maps the same pairs (a, b) -> (a + b, a - b),
-// so the fp32 sums are the definition's, whoever computes them.  The 16-byte
-// chunks are stored with their slot XORed by (block & 1) | (quarter << 1), so
-// neither the writes nor the reads of a quarter-warp share a bank.
-__device__ __forceinline__ void rotate_store(float (&v)[32], int q, float* xp, uint16_t* dst) {
-#pragma unroll
-  for (int st = 1; st < 32; st <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      if ((i & st) == 0) {
-        const float a = v[i], b = v[i + st];
-        v[i] = a + b;
-        v[i + st] = a - b;
-      }
-    }
-  }
-  const int ul = (threadIdx.x & 31) >> 2;  // block of the warp's eight
-  float* blk = xp + ul * 128;
-  __syncwarp();  // the previous pass's reads of xp are done
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int slot = i ^ ((ul & 1) | (q << 1));
-    *reinterpret_cast<float4*>(blk + q * 32 + slot * 4) = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-  }
-  __syncwarp();
-  float w[4][8];  // w[r][e] = element 32r + 8q + e
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int slot = (2 * q + h) ^ ((ul & 1) | (r << 1));
-      const float4 t = *reinterpret_cast<const float4*>(blk + r * 32 + slot * 4);
-      w[r][4 * h] = t.x;
-      w[r][4 * h + 1] = t.y;
-      w[r][4 * h + 2] = t.z;
-      w[r][4 * h + 3] = t.w;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float b0 = w[0][e] + w[1][e], b1 = w[0][e] - w[1][e];  // stride 32
-    const float b2 = w[2][e] + w[3][e], b3 = w[2][e] - w[3][e];
-    w[0][e] = b0 + b2;  // stride 64
-    w[2][e] = b0 - b2;
-    w[1][e] = b1 + b3;
-    w[3][e] = b1 - b3;
-  }
-  if (dst != nullptr) {
-    uint16_t* base = dst - 32 * q;  // the block's first element
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      uint32_t o[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        // 2^-4 is exact; both values rounded to fp16 by one conversion
-        const __half2 hv = __floats2half2_rn(w[r][2 * i] * 0.0625f, w[r][2 * i + 1] * 0.0625f);
-        o[i] = *reinterpret_cast<const uint32_t*>(&hv);
-      }
-      *reinterpret_cast<uint4*>(base + 32 * r + 8 * q) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-  }
-}
-
-// The same butterfly over eight lanes per block, 16 values a lane (elements
-// 16p..16p+15 of lane p of the eight), for the plain transform: 74 registers
-// against 110-127 for the four-lane form, so three blocks of eight warps stay
-// resident per SM instead of two (measured 3-17% faster, most at m <= 512).  Strides 1..8 run in registers; one pass through the
+// part in the exchange).  74 registers in the plain transform against 110-127
+// for a four-lane form (32 values a lane), so three blocks of eight warps stay
+// resident per SM instead of two (measured 3-17% faster, most at m <= 512).
+// Strides 1..8 run in registers; one pass through the
 // warp's shared-memory area (four blocks of 128 floats, 144 apart so the two
 // blocks of a half-warp land on different banks) regroups each lane to
 // elements 16t + 2p + e (t = 0..7, e = 0, 1), whose stride-16, -32 and -64
@@ -263,44 +196,41 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
                                                                      int64_t k, const uint16_t* __restrict__ suh,
                                                                      int num_shards, uint16_t* __restrict__ xh) {
   pdl_launch_dependents();
-  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  __shared__ __align__(16) float xpose[8][4 * 144];  // per warp: its four blocks for the stride-16..64 stages
   float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int q = lane & 3;
+  const int p = lane & 7;  // which 16 elements of the block
   const int64_t kb = k >> 7;
   const int64_t units = m * kb;
-  const int64_t groups = (units + 7) / 8;
+  const int64_t groups = (units + 3) / 4;  // four blocks per warp and pass
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
-  // the lane's unit advances by 8 * warps_total a pass: (row, block) stepped
-  const int64_t step = 8 * warps_total;
+  // the lane's unit advances by 4 * warps_total a pass: (row, block) stepped
+  const int64_t step = 4 * warps_total;
   const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
-  auto load = [&](bool ok, int64_t row, int64_t col, uint4 (&gw)[4], uint4 (&uw)[4]) {
+  auto load = [&](bool ok, int64_t row, int64_t col, uint4 (&gw)[2], uint4 (&uw)[2]) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       gw[c] = ok ? *reinterpret_cast<const uint4*>(gu + row * 2 * k + col + 8 * c) : make_uint4(0, 0, 0, 0);
       uw[c] = ok ? *reinterpret_cast<const uint4*>(gu + row * 2 * k + k + col + 8 * c) : make_uint4(0, 0, 0, 0);
     }
   };
   int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  int64_t u = g * 8 + (lane >> 2);
+  int64_t u = g * 4 + (lane >> 3);
   int64_t row = u / kb, blk = u - row * kb;
-  bool ok = g < groups && u < units;
-  int64_t col = blk * 128 + 32 * q;
-  uint4 cg[4], cu[4];
-  load(ok, row, col, cg, cu);
+  uint4 cg[2], cu[2];
+  load(g < groups && u < units, row, blk * 128 + 16 * p, cg, cu);
   for (; g < groups; g += warps_total, u += step) {
     int64_t nrow = row + step_rows, nblk = blk + step_blk;
     if (nblk >= kb) {
       nblk -= kb;
       nrow += 1;
     }
-    const int64_t ncol = nblk * 128 + 32 * q;
     const bool nok = g + warps_total < groups && u + step < units;
-    uint4 ng[4], nu[4];
-    load(nok, nrow, ncol, ng, nu);
-    float h[32];
+    uint4 ng[2], nu[2];
+    load(nok, nrow, nblk * 128 + 16 * p, ng, nu);
+    float h[16];
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint16_t ge[8], ue[8];
       unpack8(cg[c], ge);
       unpack8(cu[c], ue);
@@ -310,27 +240,26 @@ __global__ void __launch_bounds__(256) input_transform_swiglu_kernel(const uint1
         h[8 * c + i] = gv / (1.0f + expf(-gv)) * to_f32<X_BF16>(ue[i]);
       }
     }
-    const int64_t c0 = ok ? col : 32 * q;
+    const bool ok = u < units;
+    const int64_t col = ok ? blk * 128 + 16 * p : 16 * p;
     for (int s = 0; s < num_shards; ++s) {
-      float v[32];
+      float v[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint16_t se[8];
-        unpack8(*reinterpret_cast<const uint4*>(suh + (int64_t)s * k + c0 + 8 * c), se);
+        unpack8(*reinterpret_cast<const uint4*>(suh + (int64_t)s * k + col + 8 * c), se);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[8 * c + i] = h[8 * c + i] * __half2float(__ushort_as_half(se[i]));
       }
-      rotate_store(v, q, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
+      rotate_store16(v, p, xp, ok ? xh + ((int64_t)s * m + row) * k + col : nullptr);
     }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       cg[c] = ng[c];
       cu[c] = nu[c];
     }
-    ok = nok;
     row = nrow;
     blk = nblk;
-    col = ncol;
   }
 }
 
@@ -347,26 +276,26 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
     int64_t rows, int32_t topk, const int32_t* __restrict__ block_expert, int32_t block,
     const uint16_t* __restrict__ suh, int num_shards, int num_experts, uint16_t* __restrict__ xh) {
   pdl_launch_dependents();
-  __shared__ __align__(16) float xpose[8][8 * 128];  // per warp: its eight blocks for the stride-32/64 stages
+  __shared__ __align__(16) float xpose[8][4 * 144];  // per warp: its four blocks for the stride-16..64 stages
   float* const xp = xpose[threadIdx.x >> 5];
   const int lane = threadIdx.x & 31;
-  const int q = lane & 3;
+  const int p = lane & 7;  // which 16 elements of the block
   const int64_t kb = k >> 7;
   const int64_t units = rows * kb;
-  const int64_t groups = (units + 7) / 8;
+  const int64_t groups = (units + 3) / 4;  // four blocks per warp and pass
   const int64_t warps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t pairs = num_tokens * topk;
   const int block_shift = block == 16 ? 4 : block == 32 ? 5 : 7;  // block is 16, 32 or 128 rows
-  // the lane's unit advances by 8 * warps_total a pass: (row, block) stepped
-  const int64_t step = 8 * warps_total;
+  // the lane's unit advances by 4 * warps_total a pass: (row, block) stepped
+  const int64_t step = 4 * warps_total;
   const int64_t step_rows = step / kb, step_blk = step - step_rows * kb;
   int64_t g = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  int64_t u = g * 8 + (lane >> 2);
+  int64_t u = g * 4 + (lane >> 3);
   int64_t ur = u / kb, ub = u - ur * kb;
   for (; g < groups; g += warps_total, u += step) {
     const bool in_range = u < units;
     const int64_t r = in_range ? ur : 0;
-    const int64_t col = (in_range ? ub * 128 : 0) + 32 * q;
+    const int64_t col = (in_range ? ub * 128 : 0) + 16 * p;
     ub += step_blk;
     ur += step_rows;
     if (ub >= kb) {
@@ -378,19 +307,19 @@ __global__ void __launch_bounds__(256) moe_input_transform_kernel(
     const int64_t id = live ? (int64_t)sorted_ids[r] : -1;
     // pair ids stay below num_tokens * topk <= 2^28: a 32-bit division
     const int64_t tok = (id >= 0 && id < pairs) ? (int64_t)((uint32_t)id / (uint32_t)topk) : -1;
-    uint4 xw[4];
+    uint4 xw[2];
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int c = 0; c < 2; ++c)
       xw[c] = tok >= 0 ? *reinterpret_cast<const uint4*>(x + tok * k + col + 8 * c) : make_uint4(0, 0, 0, 0);
     for (int s = 0; s < num_shards; ++s) {
-      float v[32];
+      float v[16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)  // 0 on padding rows
+      for (int c = 0; c < 2; ++c)  // 0 on padding rows
         scale_chunk<X_BF16>(xw[c],
                             tok >= 0 ? *reinterpret_cast<const uint4*>(suh + ((int64_t)e * num_shards + s) * k + col + 8 * c)
                                      : make_uint4(0, 0, 0, 0),
                             v + 8 * c);
-      rotate_store(v, q, xp, live ? xh + ((int64_t)s * rows + r) * k + col : nullptr);
+      rotate_store16(v, p, xp, live ? xh + ((int64_t)s * rows + r) * k + col : nullptr);
     }
   }
 }
@@ -434,7 +363,7 @@ cudaError_t launch_input_transform(const void* x, bool x_bf16, int64_t m, int64_
 
 cudaError_t launch_input_transform_swiglu(const void* gate_up, bool bf16, int64_t m, int64_t k, const uint16_t* suh,
                                           int num_shards, uint16_t* xh, cudaStream_t stream) {
-  const int64_t groups = (m * (k >> 7) + 7) / 8;
+  const int64_t groups = (m * (k >> 7) + 3) / 4;  // one warp pass each (four blocks)
   const int threads = 256;
   const int64_t want = (groups + 7) / 8;
   const int cap = bf16 ? resident_blocks<2>(input_transform_swiglu_kernel<true>, threads)
@@ -454,7 +383,7 @@ cudaError_t launch_moe_input_transform(const void* x, bool x_bf16, int64_t num_t
                                        const int32_t* sorted_ids, int64_t rows, int32_t topk,
                                        const int32_t* block_expert, int32_t block, const uint16_t* suh,
                                        int num_shards, int num_experts, uint16_t* xh, cudaStream_t stream) {
-  const int64_t groups = (rows * (k >> 7) + 7) / 8;
+  const int64_t groups = (rows * (k >> 7) + 3) / 4;  // one warp pass each (four blocks)
   const int threads = 256;
   const int64_t want = (groups + 7) / 8;
   const int cap = x_bf16 ? resident_blocks<4>(moe_input_transform_kernel<true>, threads)

@@ -31,6 +31,7 @@ CASES = [
     (3, 6, 2, 32, 512, [384, 384], 4, 1),  # few blocks, 384-aligned shards: 96-column strips
     (4, 10, 2, 16, 256, [256], 4, 1),  # 16-row blocks (few tokens per expert)
     (7, 5, 3, 16, 384, [128, 128], 3, 2),  # 16-row blocks, odd k/128
+    (60, 4, 2, 128, 512, [256], 8, 1),  # 128-row blocks at 8 bits: two k atoms a stage
 ]
 
 

@@ -112,13 +112,57 @@ def test_input_transform_parity(xdtype):
                              f"lo {lo[tuple(i)]!r} hi {hi[tuple(i)]!r}")
 
 
+def _fp32_butterfly_fp16(x, suh):
+    """x * suh, the 128-point butterfly in fp32 (strides 1, 2, ..., 64, each
+    stage (a, b) -> (a + b, a - b) rounded to nearest even), times 2^-4, then
+    fp16 round-to-nearest-even: the transform's arithmetic written out with
+    numpy's IEEE float32, for a bit-level check of the kernels."""
+    s, k = suh.shape
+    m = x.shape[0]
+    v = (x.astype(np.float32)[None] * suh.astype(np.float32)[:, None, :]).reshape(s, m, k // 128, 128)
+    idx = np.arange(128)
+    st = 1
+    while st < 128:
+        lo = idx[(idx & st) == 0]
+        a, b = v[..., lo].copy(), v[..., lo + st].copy()
+        v[..., lo] = a + b
+        v[..., lo + st] = a - b
+        st <<= 1
+    return (v.reshape(s, m, k) * np.float32(0.0625)).astype(np.float16)
+
+
 @pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("m,k,s", [(37, 640, 3), (1, 128, 1), (300, 5120, 2)])
-def test_input_transform_bits_equal_four_lane_form(xdtype, m, k, s):
-    """The plain transform (eight lanes a block) and the grouped-expert
-    transform (four lanes a block) run the butterfly's stages in the same
-    stride order on the same pairs, so with one expert and the identity routing
-    their fp16 bytes are equal for every row and shard."""
+def test_input_transform_bits_equal_fp32_butterfly(xdtype, m, k, s):
+    """The transform's fp16 bytes equal the fixed-order fp32 butterfly written
+    out on the host (x * suh is exact in fp32, every stage rounds once, in the
+    stride order 1..64), for the plain and the gathered transform (one expert,
+    identity routing; padding rows zero)."""
+    g = torch.Generator().manual_seed(70 + m)
+    suh = (torch.rand(s, k, generator=g) * 0.4 + 0.8).to(torch.float16)
+    suh[:, ::5] = -suh[:, ::5]
+    x = synthetic.make_x(m, k, seed=71).to(xdtype)
+    want = _fp32_butterfly_fp16(x.float().numpy(), suh.float().numpy())
+    plain = E.input_transform(x.to(DEV), suh.to(DEV))
+    assert np.array_equal(plain.cpu().numpy().view(np.int16), want.view(np.int16))
+    block = 16
+    rows = (m + block - 1) // block * block
+    ids = torch.arange(rows, dtype=torch.int32)
+    ids[m:] = m  # padding rows (an id past the last pair)
+    grouped = E.moe_input_transform(x.to(DEV), ids.to(DEV), 1, torch.zeros(rows // block, dtype=torch.int32,
+                                    device=DEV), block, suh[None].to(DEV))
+    got = grouped.cpu().numpy()
+    assert np.array_equal(got[:, :m].view(np.int16), want.view(np.int16))
+    assert not got[:, m:].any()
+
+
+@pytest.mark.parametrize("xdtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("m,k,s", [(37, 640, 3), (1, 128, 1), (300, 5120, 2)])
+def test_input_transform_bits_equal_gathered_form(xdtype, m, k, s):
+    """The plain transform and the grouped-expert (gathered) transform run the
+    butterfly's stages in the same stride order on the same pairs, so with one
+    expert and the identity routing their fp16 bytes are equal for every row
+    and shard."""
     g = torch.Generator().manual_seed(60 + m)
     suh = (torch.rand(s, k, generator=g) * 0.4 + 0.8).to(torch.float16)
     suh[:, ::3] = -suh[:, ::3]
