@@ -195,11 +195,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
   for (int i = 1; i < kMaxShards; ++i)
     if (i < a.num_shards && c0 >= a.shard_cols[i]) shard = i;
+  // the first tile column of this CTA's trellis copies (a pair's CTAs decode
+  // one half of the columns each)
+  const int nt0 = (int)(c0 >> 4) + (int)prank * (C::kBNL / 16);
+  // trellis copies issued before the block synchronises (by thread 0, the
+  // producer): the first min(nk, NT) stages, whose slots start empty
+  const int npre = nk < NT ? nk : NT;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NT; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], kTcDecodeWarps);
+    }
+    // The first trellis copies go out now, while the tensor memory is
+    // allocated and the block (or pair) synchronises: they need only this
+    // CTA's own trellis barriers, initialised just above.
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    prefetch_tensormap(&maps.trellis);
+    for (int it = 0; it < npre; ++it) {
+      mbar_arrive_expect_tx(&tfull[it], (uint32_t)C::kTrCopy);
+      tma_tile3d_g2s(rings + C::kTRing + it * C::kTSlot, &maps.trellis, 0, nt0, (int)(kb0 + (int64_t)it * KA) * 4,
+                     &tfull[it]);
     }
     for (int s = 0; s < NX; ++s) {
       mbar_init(&xfull[s], 1);
@@ -232,11 +249,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     // ---------------- trellis producer ----------------
     if (lane == 0) {
-      prefetch_tensormap(&maps.trellis);
-      const int nt0 = (int)(c0 >> 4) + (int)prank * (C::kBNL / 16);
-      int s = 0;
-      uint32_t ph = 0;
-      for (int it = 0; it < nk; ++it) {
+      // the first npre stages went out before the block synchronised
+      int s = npre == NT ? 0 : npre;
+      uint32_t ph = npre == NT ? 1u : 0u;
+      for (int it = npre; it < nk; ++it) {
         if (!mbar_wait(&tempty[s], ph ^ 1u)) break;
         mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);  // first 64-wide k atom of the stage
