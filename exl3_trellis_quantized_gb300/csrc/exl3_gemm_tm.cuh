@@ -239,11 +239,34 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   const int64_t stride = gridDim.x;
   // this CTA's items: blockIdx.x, blockIdx.x + G, ...
   const int64_t count = (items - blockIdx.x + stride - 1) / stride;
+  // Dense calls: the trellis copies of the first min(nk, NT) stages of this
+  // CTA's first item (item blockIdx.x, always live) are issued by thread 0,
+  // the producer, before the block synchronises; their slots start empty.
+  int npre = 0;
+  int64_t first_c0 = 0, first_kb0 = 0;
+  if constexpr (!MOE) {
+    const TmItem first = tm_item<KA, false>(a, blockIdx.x);
+    npre = first.nk < NT ? first.nk : NT;
+    first_c0 = first.c0;
+    first_kb0 = first.kb0;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NT; ++s) {
       mbar_init(&tfull[s], 1);
       mbar_init(&tempty[s], kTmDecodeWarps);
+    }
+    if constexpr (!MOE) {
+      // they need only the trellis barriers, initialised just above, and
+      // overlap the tensor-memory allocation and the block barrier
+      fence_mbar_init();
+      fence_proxy_async_smem();
+      prefetch_tensormap(&maps.trellis);
+      for (int it = 0; it < npre; ++it) {
+        mbar_arrive_expect_tx(&tfull[it], (uint32_t)C::kTrCopy);
+        tma_tile3d_g2s(rings + C::kTRing + it * C::kTSlot, &maps.trellis, 0, (int)(first_c0 >> 4),
+                       (int)(first_kb0 + (int64_t)it * KA) * 4, &tfull[it]);
+      }
     }
     for (int s = 0; s < NX; ++s) {
       mbar_init(&xfull[s], 1);
@@ -274,15 +297,16 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   if (warp == 0) {
     // ---------------- trellis producer ----------------
     if (lane == 0) {
-      prefetch_tensormap(&maps.trellis);
-      int s = 0;
-      uint32_t ph = 0;
+      if constexpr (MOE) prefetch_tensormap(&maps.trellis);
+      // the first npre stages went out before the block synchronised
+      int s = npre == NT ? 0 : npre;
+      uint32_t ph = npre == NT ? 1u : 0u;
       bool ok = true;
       for (int64_t i = 0; ok && i < count; ++i) {
         const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
         if (!t.live) continue;
         const int nt0 = (int)(t.c0 >> 4);
-        for (int it = 0; it < t.nk; ++it) {
+        for (int it = i == 0 ? npre : 0; it < t.nk; ++it) {
           if (!mbar_wait(&tempty[s], ph ^ 1u)) {
             ok = false;
             break;
