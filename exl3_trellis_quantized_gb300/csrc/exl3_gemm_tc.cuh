@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // the first npre stages went out before the block synchronised
       int s = npre == NT ? 0 : npre;
       uint32_t ph = npre == NT ? 1u : 0u;
-      for (int it = npre; it < nk; ++it) {
+      int it = npre;
+      for (; it < nk; ++it) {
         if (!mbar_wait(&tempty[s], ph ^ 1u)) break;
         mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);  // first 64-wide k atom of the stage
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ph ^= 1u;
         }
       }
+      drain_ring(tfull, NT, it);  // it copies issued
     }
   } else if (warp == 2) {
     // ---------------- activation producer ----------------
@@ -277,7 +279,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t tx = (uint32_t)(RG * KA) * (uint32_t)p.box_rows * 128u;
       int s = 0;
       uint32_t ph = 0;
-      for (int it = 0; it < nk; ++it) {
+      int it = 0;
+      for (; it < nk; ++it) {
         if (!mbar_wait(&xempty[s], ph ^ 1u)) break;
         mbar_arrive_expect_tx(&xfull[s], tx);
         const int atom0 = (int)(kb0 + (int64_t)it * KA);
@@ -300,6 +303,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ph ^= 1u;
         }
       }
+      drain_ring(xfull, NX, it);  // it copies issued
     }
   } else if (warp == 3) {
     // ---------------- sender (pairs) ----------------

@@ -94,7 +94,9 @@ struct TmCfg {
   static_assert(kNW >= 2 && kNT >= 3, "rings too shallow");
   static_assert(kABase + kNW * kACols <= 512, "tensor memory overflow");
   static_assert(kXSlot % 1024 == 0, "activation slots keep 1024-byte swizzle alignment");
-  static_assert((2 * kNT + 2 * kNX + 2 * kNW + 4) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
+  // the rings' full and empty barriers, accfull[2], accempty[2], zfull, zdone
+  // and mdrain, then the tensor-memory address and the failure flag
+  static_assert((2 * kNT + 2 * kNX + 2 * kNW + 7) * 8 + 8 <= kCtrlBytes, "barriers exceed the control area");
 };
 
 // State of relative value D of a thread's window from its aligned views
@@ -227,7 +229,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   uint64_t* accempty = accfull + 2;                     // [2] an item's accumulator read by the epilogue
   uint64_t* zfull = accempty + 2;                       // the epilogue staging tile written by all four warps
   uint64_t* zdone = zfull + 1;                          // the epilogue staging tile read by all four warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(zdone + 1);
+  uint64_t* mdrain = zdone + 1;                         // the MMAs issued before a wait gave up are done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mdrain + 1);
   volatile uint32_t* failed = tmem_slot + 1;  // set by the MMA issuer if a wait gave up
   uint8_t* rings = base + C::kCtrlBytes;
 
@@ -282,6 +285,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     }
     mbar_init(zfull, 4);
     mbar_init(zdone, 4);
+    mbar_init(mdrain, 1);
     *failed = 0u;
     fence_mbar_init();
   }
@@ -301,6 +305,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       // the first npre stages went out before the block synchronised
       int s = npre == NT ? 0 : npre;
       uint32_t ph = npre == NT ? 1u : 0u;
+      int64_t issued = npre;  // copies put into the ring so far
       bool ok = true;
       for (int64_t i = 0; ok && i < count; ++i) {
         const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
@@ -311,6 +316,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             ok = false;
             break;
           }
+          ++issued;
           mbar_arrive_expect_tx(&tfull[s], (uint32_t)C::kTrCopy);
           if constexpr (MOE) {
             tma_tile4d_g2s(rings + C::kTRing + s * C::kTSlot, &maps.trellis, 0, nt0,
@@ -325,6 +331,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           }
         }
       }
+      drain_ring(tfull, NT, issued);
     }
   } else if (warp == 2) {
     // ---------------- activation producer ----------------
@@ -337,6 +344,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       const uint32_t tx = (uint32_t)KA * (uint32_t)p.box_rows * 128u;
       int s = 0;
       uint32_t ph = 0;
+      int64_t issued = 0;  // copies put into the ring so far
       bool ok = true;
       for (int64_t i = 0; ok && i < count; ++i) {
         const TmItem t = tm_item<KA, MOE>(a, blockIdx.x + i * stride);
@@ -350,6 +358,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
             ok = false;
             break;
           }
+          ++issued;
           mbar_arrive_expect_tx(&xfull[s], tx);
           const int atom0 = (int)(t.kb0 + (int64_t)it * KA);
           if (p.box_rows == XR) {
@@ -368,6 +377,7 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           }
         }
       }
+      drain_ring(xfull, NX, issued);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
@@ -427,7 +437,16 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         __syncwarp();
         ++li;
       }
-      if (!ok && leader) *failed = 1u;
+      if (!ok) {
+        // a wait gave up: the MMAs issued so far may still be running, so
+        // wait (bounded) for them before the tensor memory is freed
+        if (leader) {
+          *failed = 1u;
+          tc_commit(mdrain);
+        }
+        __syncwarp();
+        mbar_wait(mdrain, 0u);
+      }
     }
     __syncwarp();
   } else if (warp >= kTmFirstDecoder && warp < kTmFirstEpilogue) {

@@ -93,6 +93,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+// After a producer's loop: wait until the last min(issued, n) copies it put
+// into a ring of n slots have landed (copy j went to slot j % n and completes
+// the phase of parity (j / n) & 1 of that slot's full barrier), so that no copy
+// still writes into shared memory when the CTA exits.  In a normal run the
+// consumers have already waited for every one of them, so each wait returns at
+// once; after a wait of the kernel gave up, each is bounded like every wait,
+// and the first that gives up ends the drain.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int n, int64_t issued) {
+  for (int64_t j = issued > n ? issued - n : 0; j < issued; ++j)
+    if (!mbar_wait(&full[j % n], (uint32_t)(j / n) & 1u)) return;
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 1-D bulk copy and 3-D tiled tensor copy, completing on an mbarrier.
 // ---------------------------------------------------------------------------
