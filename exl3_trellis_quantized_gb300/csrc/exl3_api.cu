@@ -165,8 +165,10 @@ exl3_status_t exl3_gemm(const uint16_t* xh, int64_t m, int64_t k, const int16_t*
 // Shape-only split policy: the number of parts P makes (n/128) * P work units
 // fill the 152 SMs of a GB300 in whole waves as evenly as possible.  It is the
 // smallest P whose wave efficiency units / (152 * ceil(units / 152)) reaches
-// 0.85, else the most efficient P; P <= k/128 (parts are whole 128-row blocks)
-// and P <= 16.  It never depends on m, so rows are byte-equal across batches.
+// 0.85, else the most efficient P; P <= k/128 (every part holds at least one
+// 128-row block; split_part_atoms picks whole 256-row units where k/128 is
+// even and P <= k/256) and P <= 16.  It never depends on m, so rows are
+// byte-equal across batches.
 int32_t exl3_splitk_parts(int64_t k, int64_t n) {
   if (!valid_kn(k) || !valid_kn(n)) return 0;
   const int64_t nb = n / 128;

@@ -128,17 +128,17 @@ enum class TcShape : int {
   // Decoded weights as the tensor core's A operand (M = 128 weight columns),
   // the XR activation rows as B (N = XR): kT* keep A in tensor memory
   // (exl3_gemm_tm.cuh), kS* in shared memory (strips in clusters of four).
-  kT128K4,       // BN=128, KA=4, XR=32 (m <= 32, k/128 even, no split-k)
+  kT128K4,       // BN=128, KA=4, XR=32 (m <= 32, k/128 even; split-k only on 256-row parts)
   kT128,         // BN=128, KA=2, XR=32 (m <= 32)
   kS96K4,        // BN=96,  KA=4, XR=32 (m <= 32, k/128 even, no split-k, n and shard edges multiples of 384)
-  kT128K4X16,    // BN=128, KA=4, XR=16 (m <= 16, k/128 even, no split-k)
+  kT128K4X16,    // BN=128, KA=4, XR=16 (m <= 16, k/128 even; split-k only on 256-row parts)
   kS96K4X16,     // BN=96,  KA=4, XR=16 (m <= 16, k/128 even, no split-k, 384-aligned edges)
   kT128X16,      // BN=128, KA=2, XR=16 (m <= 16)
-  kT128K4X64,    // BN=128, KA=4, XR=64 (m <= 64, k/128 even, no split-k)
+  kT128K4X64,    // BN=128, KA=4, XR=64 (m <= 64, k/128 even; split-k only on 256-row parts)
   kT128X64,      // BN=128, KA=2, XR=64 (m <= 64)
   kT128X128,     // BN=128, KA=2, XR=128 (m <= 128)
   kS96K4X64,     // BN=96,  KA=4, XR=64 (m <= 64, k/128 even, no split-k, 384-aligned edges)
-  kT128K4X128,   // BN=128, KA=4 (2 at 7-8 bits), XR=128 (m <= 128, k/128 even)
+  kT128K4X128,   // BN=128, KA=4 (2 at 7-8 bits), XR=128 (m <= 128, k/128 even; split-k only on 256-row parts)
   kLast = kT128K4X128,
 };
 // Runs the whole GEMM (parts == 1) or writes the fp32 partials of every part
