@@ -1,8 +1,9 @@
 // exl3_gemm_tm.cuh -- small-batch EXL3 GEMM with the decoded weights in tensor
 // memory.
 //
-// One CTA owns 128 output columns (one Hadamard block) and at most XR <= 32
-// batch rows, over all of k or one shape-fixed part of it.  The tensor core
+// A work item is 128 output columns (one Hadamard block) and at most XR batch
+// rows (XR = 16, 32, 64 or 128), over all of k or one shape-fixed part of it;
+// in the grouped (MOE) mode, one expert block's rows.  The tensor core
 // takes the decoded weights as its A operand (M = 128 weight columns) straight
 // from tensor memory and the rotated activations as B (N = XR rows) from
 // shared memory: the accumulator holds one weight column per tensor-memory
@@ -26,12 +27,12 @@
 // decode (two accumulator buffers in tensor memory).
 //
 // Warp roles: 0 trellis producer (3-D tensor copies into a deep ring), 1 MMA
-// issuer (lane 0), 2 activation producer, 3 idle, 4..19 decoders, 20..23 the
-// epilogue.  Decoder warp dw serves lane quarter dw & 3 (a warp reaches only
-// the tensor-memory lanes of its sub-partition) and the stage's k16 rows
-// (dw >> 2) + 4i; epilogue warp e reads lane quarter e.  Tensor memory: the
-// two accumulators in columns [0, 32) and [32, 64), NW slots of decoded A
-// (32*KA columns each) from column 128.
+// issuer (one elected lane), 2 activation producer, 3 idle, 4..19 decoders,
+// 20..23 the epilogue.  Decoder warp dw serves lane quarter dw & 3 (a warp
+// reaches only the tensor-memory lanes of its sub-partition) and the stage's
+// k16 rows (dw >> 2) + 4i; epilogue warp e reads lane quarter e.  Tensor
+// memory: two accumulators of max(32, XR) columns from column 0, then NW slots
+// of decoded A (32*KA columns each) from column max(128, 2 * max(32, XR)).
 #pragma once
 
 #include "exl3_device.cuh"
