@@ -24,13 +24,15 @@
 //
 // Warp roles:
 //   warp 0      trellis producer: one 3-D tensor copy per stage of the CTA's
-//               tiles for the stage's k16 rows;
+//               tiles for the stage's k16 rows (thread 0 issues the first
+//               ring-full before the block synchronises);
 //   warp 1      TMEM allocator and MMA issuer: the warp runs the loop and
 //               one elected lane issues tcgen05.mma kind::f16 (M=128, N=BN,
 //               K=16) per row group and k16 step, fp32 accumulators in tensor
 //               memory (with SWAP, M=128 weight columns and N=XR rows);
 //   warp 2      activation producer: one 4-D tensor copy of xh (KA atoms,
-//               128-byte swizzle) per row group and stage;
+//               128-byte swizzle) per row group and stage, or one per atom of
+//               just the rows in use when the batch is smaller than a slot;
 //   warp 3      with PAIR = 2, sends the CTA's decoded half of each stage to
 //               the partner (bulk copy into its shared memory);
 //   warps 4..19 decoders: each lane decodes its 8 values of a 16x16 tile
@@ -39,10 +41,11 @@
 //               stmatrix stores them into the 128-byte-swizzled K-major B
 //               operand; then the epilogue.
 //
-// Small batches: the activation region of an atom holds only XR rows.  The
-// tensor core still reads 128 rows; rows past XR land on later bytes of the
-// rings, which only feed accumulator rows that are never stored.  The read
-// span always stays inside the rings.
+// Small batches: the activation region of an atom holds only XR rows, and the
+// copies leave rows past the batch unwritten.  The tensor core still reads 128
+// (or, for the 64-row MMA, 64) rows; rows past the batch, or past XR on later
+// bytes of the rings, only feed accumulator rows that are never stored.  The
+// read span always stays inside the rings.
 //
 // Each tile is decoded exactly once per CTA (per pair with PAIR = 2).  The fp32
 // sum over k is a fixed sequence of tcgen05 k16 steps in ascending k for every
