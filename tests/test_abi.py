@@ -96,6 +96,38 @@ def test_splitk_rejects_small_workspace(L):
     assert st == 3
 
 
+def _shape_call(L, shape, m, k, n, split=False):
+    cols = (ctypes.c_int32 * 2)(0, n)
+    v = ctypes.c_void_p(FAKE)
+    acc = v if split else None
+    nbytes = L.exl3_splitk_workspace_bytes(m, k, n) if split else 0
+    return L.exl3_test_gemm_shape(shape, v, m, k, v, 4, 1, v, cols, 1, v, 1, n, acc, nbytes, None)
+
+
+@pytest.mark.parametrize("shape,m,k,n,split", [
+    (18, 8, 1024, 512, True),     # four-atom tensor-memory tiles on 128-row parts (P = 8 > k/256)
+    (21, 8, 1024, 512, True),
+    (28, 8, 1024, 512, True),
+    (18, 33, 1024, 512, False),   # more rows than the shape holds
+    (21, 17, 1024, 512, False),
+    (28, 129, 1024, 512, False),
+    (28, 64, 384, 512, False),    # odd k/128: no four-atom stages
+    (8, 8, 1024, 4864, True),     # shared-memory four-atom tiles never run split-k parts, even 256-row ones
+    (12, 8, 2048, 4096, True),
+])
+def test_tile_shape_support_rules(L, shape, m, k, n, split):
+    """Host-side shape checks of exl3_test_gemm_shape: a shape that cannot run
+    the call returns EXL3_EUNSUPPORTED before any launch (no GPU needed)."""
+    if split:
+        assert L.exl3_splitk_parts(k, n) > 1
+    assert _shape_call(L, shape, m, k, n, split) == 2
+
+
+def test_tile_shape_out_of_range(L):
+    assert _shape_call(L, B.TEST_TILE_SHAPES, 8, 1024, 512) == 1
+    assert _shape_call(L, -2, 8, 1024, 512) == 1
+
+
 def test_input_transform_rejects_invalid(L):
     v = ctypes.c_void_p(FAKE)
     assert L.exl3_input_transform(v, 1, 4, 200, v, 1, v, None) == 1
