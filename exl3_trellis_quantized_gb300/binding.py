@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
     L.exl3_test_tile_plan.argtypes = [i64, i64, i64, ctypes.POINTER(ctypes.c_int32), i32, i32,
                                       ctypes.POINTER(ctypes.c_int64)]
     L.exl3_test_tile_plan.restype = ctypes.c_int
+    L.exl3_test_wait_timeout.argtypes = [vp, vp]
+    L.exl3_test_wait_timeout.restype = ctypes.c_int
     L.exl3_set_autotune.argtypes = [i32]
     L.exl3_set_autotune.restype = ctypes.c_int
     L.exl3_clear_autotune.argtypes = []
@@ -90,6 +92,14 @@ def device_status() -> int:
     flags = ctypes.c_uint32(0)
     _check(lib().exl3_device_status(ctypes.byref(flags)), "exl3_device_status")
     return int(flags.value)
+
+
+def test_wait_timeout(device="cuda") -> int:
+    """exl3_test_wait_timeout: a kernel whose bounded wait gives up (about 2 s);
+    returns the kernel's out word (0 when the wait gave up)."""
+    out = torch.full((1,), 7, dtype=torch.int32, device=device)
+    _check(lib().exl3_test_wait_timeout(_ptr(out), _stream(out)), "exl3_test_wait_timeout")
+    return int(out.item())
 
 
 def test_tile_plan(m: int, k: int, n: int, shard_cols: Sequence[int], split: bool = False) -> tuple:

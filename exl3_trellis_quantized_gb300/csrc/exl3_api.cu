@@ -297,6 +297,12 @@ const char* exl3_status_string(exl3_status_t status) {
 
 const char* exl3_last_error(void) { return g_last_error; }
 
+exl3_status_t exl3_test_wait_timeout(uint32_t* out, void* stream) {
+  if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 3u) != 0) return EXL3_EINVAL;
+  return cuda_status(exl3::launch_test_wait_timeout(out, static_cast<cudaStream_t>(stream)),
+                     "exl3_test_wait_timeout");
+}
+
 exl3_status_t exl3_device_status(uint32_t* flags) {
   if (flags == nullptr) return EXL3_EINVAL;
   return cuda_status(exl3::take_device_errors(flags), "exl3_device_status");

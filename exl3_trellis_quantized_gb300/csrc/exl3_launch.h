@@ -183,6 +183,8 @@ template <int BITS>
 cudaError_t launch_moe_gemm_tc_bits(const TcMaps& maps, const TcParams& p, int cb, int tile, cudaStream_t stream);
 // Read and clear the wait-timeout flags of every kernel translation unit (synchronous).
 cudaError_t take_device_errors(uint32_t* flags);
+// exl3_test_wait_timeout's kernel (in the 1-bit instantiation unit).
+cudaError_t launch_test_wait_timeout(uint32_t* out, cudaStream_t stream);
 template <int BITS>
 cudaError_t take_device_error_tc(uint32_t* flags);
 

@@ -401,6 +401,17 @@ int64_t exl3_autotune_entries(void);
 #define EXL3_DEVERR_WAIT_TIMEOUT 1u
 exl3_status_t exl3_device_status(uint32_t* flags);
 
+/*
+ * exl3_test_wait_timeout -- test-only: the failure path of the bounded waits.
+ * One CTA waits, with the same bounded mbarrier wait every kernel of the
+ * library uses, on a barrier that nothing arrives on.  The wait gives up after
+ * 2 s, the kernel sets EXL3_DEVERR_WAIT_TIMEOUT (read by exl3_device_status)
+ * and writes *out = 0 (1 would mean the wait had returned).  It faults
+ * nothing and leaves the context usable.  No counterpart in the pages.
+ *   out: device uint32, 4-byte aligned; EXL3_EINVAL when null or misaligned.
+ */
+exl3_status_t exl3_test_wait_timeout(uint32_t* out, void* stream);
+
 /* Static text for a status code. */
 const char* exl3_status_string(exl3_status_t status);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */

@@ -186,6 +186,8 @@ def test_moe_combine_rejects_invalid(L):
 
 def test_test_entry_points_reject_invalid(L):
     v = ctypes.c_void_p(FAKE)
+    assert L.exl3_test_wait_timeout(None, None) == 1
+    assert L.exl3_test_wait_timeout(ctypes.c_void_p(FAKE + 2), None) == 1  # misaligned
     assert L.exl3_test_codebook(7, v, None) == 1
     assert L.exl3_test_unpack(v, 9, 0, 64, 64, v, None) == 1
     assert L.exl3_test_unpack(v, 3, 0, 40, 64, v, None) == 1
